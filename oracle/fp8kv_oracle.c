@@ -1,0 +1,409 @@
+/*
+ * fp8kv_oracle.c -- plain, slow CPU oracle of the FP8 paged-KV decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, calls or
+ * includes this file; only the test suite, the package entry's smoke check and
+ * the CPU-baseline leg of the benchmark load it.  It shares no header, helper,
+ * table or constant with the CUDA path.
+ *
+ * What the method computes (sources are the five web pages reporting the
+ * Cloudflare Workers AI write-up on serving Kimi K2.6 / GLM 5.2):
+ *
+ *  - "Il serving di modelli piu piccoli di Cloudflare riduce la memoria, ma la
+ *    sicurezza diventa la prova decisiva" (remio.ai, Italian edition),
+ *    section "Cosa ha cambiato Cloudflare per Kimi e GLM": the Kimi KV cache is
+ *    held as FP8 e4m3 instead of BF16 (half the bytes); every physical cache
+ *    page carries a tag that changes whenever the page is reallocated; the
+ *    server records which pages and tags each request expects; the mappings
+ *    are checked before supported decode operations read the pages, and a
+ *    mismatch aborts the affected request.
+ *  - same page, section "Perche le cache piu piccole di Cloudflare battono la
+ *    velocita pura": the attention kernel converts the cached values when it
+ *    reads them.
+ *  - same page, section "La sicurezza della cache KV condivisa diventa una
+ *    questione di produzione": paged attention splits the cache into reusable
+ *    blocks with a logical-to-physical mapping per sequence; the check runs as
+ *    a separate batched operation, not fused into attention; tags behave like
+ *    generation counters.
+ *  - "Cloudflare uskorila Kimi na 41% szhatiem KV-kesha" (iitog.ru), the
+ *    paragraph on the third technique: many requests both read and write the
+ *    pages of one physical cache.
+ *
+ * The pages fix neither formulas nor layouts.  Readings taken here (each one
+ * is listed in the design notes of the repository):
+ *   e4m3 = OCP OFP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ *   bits, no infinities, NaN = S.1111.111, largest finite 448); encoding is
+ *   round-to-nearest-even with saturation to +-448; NaN encodes as 0x7F;
+ *   quantisation divides by a per-tensor fp32 scale in IEEE fp32 first;
+ *   the softmax scale is an explicit argument (1/sqrt(D) in the workloads);
+ *   query head h reads kv head h / (Hq/Hkv); tags are uint32 compared for
+ *   equality and bumped by +1 modulo 2^32; a page id outside [0, num_pages)
+ *   aborts; only the first ceil(L/page_size) entries of a page table are
+ *   checked; an aborted or empty request yields out = 0, lse = -inf.
+ *
+ * Pool layout (the library's documented storage format, restated here from
+ * its definition, not shared with it):
+ *   K pool: [num_pages][Hkv][page_size][D]                  (token-major)
+ *   V pool: [num_pages][Hkv][page_size/16][D][16]            (16-token column
+ *           blocks, each block dim-major)
+ *   element = 1 byte (e4m3 code) or 2 bytes (bf16 bit pattern).
+ *
+ * All floating point is fp64 except the single fp32 division x/scale that the
+ * quantiser is defined on.  Build with -ffp-contract=off.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* bf16 and e4m3 codecs                                                       */
+/* ------------------------------------------------------------------------- */
+
+/* bf16 is the upper half of an IEEE binary32 bit pattern. */
+static float bf16_bits_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* E4M3 decode: e == 0 -> (-1)^s * m * 2^-9 (subnormal),
+ * else (-1)^s * (1 + m/8) * 2^(e-7); S.1111.111 is NaN. */
+double orc_e4m3_decode(uint8_t code)
+{
+    int s = (code >> 7) & 1;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double mag;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* E4M3 encode of an fp32 value: round to nearest, ties to even, saturate
+ * finite and infinite overflow to +-448, NaN -> 0x7F, -0 -> 0x80. */
+uint8_t orc_e4m3_encode(float xf)
+{
+    double x = (double)xf;
+    uint8_t sign;
+    double a;
+    int code;
+
+    if (isnan(x))
+        return 0x7F;
+    sign = signbit(x) ? 0x80 : 0x00;
+    a = fabs(x);
+    if (isinf(a))
+        return (uint8_t)(sign | 0x7E);
+
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal binade: multiples of 2^-9; q == 8 is the smallest normal */
+        double q = nearbyint(a * 512.0);
+        code = (int)q;
+    } else {
+        int e2;
+        double f = frexp(a, &e2);          /* a = f * 2^e2, f in [0.5, 1) */
+        int E = e2 - 1;                    /* a = (2f) * 2^E, 2f in [1, 2) */
+        double mant = nearbyint((2.0 * f - 1.0) * 8.0);
+        int field;
+        if (mant >= 8.0) {                 /* rounding carried into the exponent */
+            mant = 0.0;
+            E += 1;
+        }
+        field = E + 7;
+        if (field > 15 || (field == 15 && mant > 6.0))
+            code = 0x7E;                   /* saturate to 448 */
+        else
+            code = (field << 3) | (int)mant;
+    }
+    return (uint8_t)(sign | code);
+}
+
+void orc_e4m3_encode_array(const float *x, int64_t n, uint8_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = orc_e4m3_encode(x[i]);
+}
+
+void orc_e4m3_decode_array(const uint8_t *c, int64_t n, double *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = orc_e4m3_decode(c[i]);
+}
+
+/* The quantiser input: float(bf16 x) / scale as one IEEE fp32 division. */
+uint8_t orc_quantize_bf16(uint16_t xbits, float scale)
+{
+    volatile float num = bf16_bits_to_float(xbits);
+    volatile float q = num / scale;
+    return orc_e4m3_encode(q);
+}
+
+void orc_quantize_bf16_array(const uint16_t *xbits, int64_t n, float scale, uint8_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = orc_quantize_bf16(xbits[i], scale);
+}
+
+/* ------------------------------------------------------------------------- */
+/* pool indexing (the documented layout)                                      */
+/* ------------------------------------------------------------------------- */
+
+static int64_t k_index(int64_t page, int h, int off, int d, int Hkv, int ps, int D)
+{
+    return ((page * Hkv + h) * (int64_t)ps + off) * D + d;
+}
+
+static int64_t v_index(int64_t page, int h, int off, int d, int Hkv, int ps, int D)
+{
+    int blk = off / 16, col = off % 16;
+    return (((page * Hkv + h) * (int64_t)(ps / 16) + blk) * D + d) * 16 + col;
+}
+
+/* ------------------------------------------------------------------------- */
+/* writing tokens into pages                                                  */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Write one token's K and V rows (all Hkv heads) of request r at position pos.
+ * The destination page's tag is compared first; a page id out of range, a
+ * position beyond the page table or a stale tag skips the write and marks the
+ * request in abort_mask (when given).  Returns 1 if written, 0 if skipped.
+ */
+static int write_token(const uint16_t *krow, const uint16_t *vrow, int is_fp8,
+                       void *k_pool, void *v_pool, float k_scale, float v_scale,
+                       const int32_t *page_table, int max_pages, int r, int pos,
+                       const uint32_t *live_tags, const uint32_t *expected_tags,
+                       uint8_t *abort_mask, int Hkv, int D, int ps, int num_pages)
+{
+    int pi = pos / ps, off = pos % ps, h, d;
+    int32_t page;
+    if (pos < 0 || pi >= max_pages) {
+        if (abort_mask) abort_mask[r] = 1;
+        return 0;
+    }
+    page = page_table[(int64_t)r * max_pages + pi];
+    if (page < 0 || page >= num_pages) {
+        if (abort_mask) abort_mask[r] = 1;
+        return 0;
+    }
+    if (live_tags && expected_tags &&
+        live_tags[page] != expected_tags[(int64_t)r * max_pages + pi]) {
+        if (abort_mask) abort_mask[r] = 1;
+        return 0;
+    }
+    for (h = 0; h < Hkv; ++h) {
+        for (d = 0; d < D; ++d) {
+            uint16_t kb = krow[(int64_t)h * D + d], vb = vrow[(int64_t)h * D + d];
+            int64_t ki = k_index(page, h, off, d, Hkv, ps, D);
+            int64_t vi = v_index(page, h, off, d, Hkv, ps, D);
+            if (is_fp8) {
+                ((uint8_t *)k_pool)[ki] = orc_quantize_bf16(kb, k_scale);
+                ((uint8_t *)v_pool)[vi] = orc_quantize_bf16(vb, v_scale);
+            } else {
+                ((uint16_t *)k_pool)[ki] = kb;
+                ((uint16_t *)v_pool)[vi] = vb;
+            }
+        }
+    }
+    return 1;
+}
+
+/*
+ * Decode-step append: one new token per request, written at position
+ * seq_lens[r] - 1 (seq_lens already counts the new token).  Requests with
+ * seq_lens[r] <= 0 append nothing.  k_new, v_new: bf16 [B][Hkv][D].
+ */
+void orc_kv_append(const uint16_t *k_new, const uint16_t *v_new, int is_fp8,
+                   void *k_pool, void *v_pool, float k_scale, float v_scale,
+                   const int32_t *page_table, int max_pages, const int32_t *seq_lens,
+                   const uint32_t *live_tags, const uint32_t *expected_tags,
+                   uint8_t *abort_mask, int B, int Hkv, int D, int ps, int num_pages)
+{
+    int r;
+    for (r = 0; r < B; ++r) {
+        int L = seq_lens[r];
+        if (L <= 0)
+            continue;
+        write_token(k_new + (int64_t)r * Hkv * D, v_new + (int64_t)r * Hkv * D, is_fp8,
+                    k_pool, v_pool, k_scale, v_scale, page_table, max_pages, r, L - 1,
+                    live_tags, expected_tags, abort_mask, Hkv, D, ps, num_pages);
+    }
+}
+
+/*
+ * Bulk write of whole prompts: rows cu_seqlens[r] .. cu_seqlens[r+1]-1 of
+ * k, v (bf16 [N][Hkv][D]) are request r's tokens at positions 0, 1, ...
+ */
+void orc_kv_prefill(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens, int is_fp8,
+                    void *k_pool, void *v_pool, float k_scale, float v_scale,
+                    const int32_t *page_table, int max_pages,
+                    const uint32_t *live_tags, const uint32_t *expected_tags,
+                    uint8_t *abort_mask, int B, int Hkv, int D, int ps, int num_pages)
+{
+    int r, i;
+    for (r = 0; r < B; ++r) {
+        for (i = cu_seqlens[r]; i < cu_seqlens[r + 1]; ++i) {
+            write_token(k + (int64_t)i * Hkv * D, v + (int64_t)i * Hkv * D, is_fp8,
+                        k_pool, v_pool, k_scale, v_scale, page_table, max_pages, r,
+                        i - cu_seqlens[r], live_tags, expected_tags, abort_mask,
+                        Hkv, D, ps, num_pages);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* page tags                                                                  */
+/* ------------------------------------------------------------------------- */
+
+/* Reallocation: each listed page's tag advances by one, modulo 2^32.  Ids
+ * outside [0, num_pages) are ignored; a repeated id advances once per entry. */
+void orc_page_tags_bump(uint32_t *live_tags, const int32_t *pages, int n, int num_pages)
+{
+    int i;
+    for (i = 0; i < n; ++i) {
+        int32_t p = pages[i];
+        if (p >= 0 && p < num_pages)
+            live_tags[p] = live_tags[p] + 1u;
+    }
+}
+
+/*
+ * Batched check before the pages are read: request r is aborted iff one of
+ * its first P_r = ceil(seq_lens[r] / ps) table entries names a page outside
+ * [0, num_pages) or a page whose live tag differs from the expected tag, or
+ * P_r exceeds the table width.  abort_mask is overwritten; returns the count.
+ */
+int orc_page_tags_validate(const int32_t *page_table, const uint32_t *expected_tags,
+                           const int32_t *seq_lens, int max_pages,
+                           const uint32_t *live_tags, int num_pages, int B, int ps,
+                           uint8_t *abort_mask)
+{
+    int r, i, count = 0;
+    for (r = 0; r < B; ++r) {
+        int L = seq_lens[r];
+        int P = L > 0 ? (L + ps - 1) / ps : 0;
+        int bad = 0;
+        if (P > max_pages)
+            bad = 1;
+        for (i = 0; i < P && !bad; ++i) {
+            int32_t page = page_table[(int64_t)r * max_pages + i];
+            if (page < 0 || page >= num_pages)
+                bad = 1;
+            else if (live_tags[page] != expected_tags[(int64_t)r * max_pages + i])
+                bad = 1;
+        }
+        abort_mask[r] = (uint8_t)bad;
+        count += bad;
+    }
+    return count;
+}
+
+/* ------------------------------------------------------------------------- */
+/* attention                                                                  */
+/* ------------------------------------------------------------------------- */
+
+static double load_k(const void *pool, int is_fp8, int64_t idx, double scale)
+{
+    if (is_fp8)
+        return orc_e4m3_decode(((const uint8_t *)pool)[idx]) * scale;
+    return (double)bf16_bits_to_float(((const uint16_t *)pool)[idx]);
+}
+
+/*
+ * Decode attention over the paged cache, fp64, no splitting.
+ * For request r and query head h (kv head h / G):
+ *   s_j = sm_scale * sum_d q[d] * khat_j[d],      j < L_r
+ *   out = sum_j exp(s_j - m) vhat_j / sum_j exp(s_j - m),  m = max_j s_j
+ *   lse = m + log(sum_j exp(s_j - m))
+ * khat = decode(code) * k_scale for the FP8 cache, the bf16 value otherwise.
+ * Aborted (abort_mask[r] != 0), empty, over-long or out-of-range-page requests
+ * give out = 0, lse = -inf.  scores: caller scratch of >= max_pages*ps doubles.
+ */
+void orc_paged_attention(const uint16_t *q, const void *k_pool, const void *v_pool, int is_fp8,
+                         double k_scale, double v_scale, const int32_t *page_table, int max_pages,
+                         const int32_t *seq_lens, const uint8_t *abort_mask, double sm_scale,
+                         int B, int Hq, int Hkv, int D, int ps, int num_pages,
+                         double *scores, double *out, double *lse)
+{
+    int r, h, j, d;
+    int G = Hq / Hkv;
+    for (r = 0; r < B; ++r) {
+        int L = seq_lens[r];
+        int P = L > 0 ? (L + ps - 1) / ps : 0;
+        int dead = (L <= 0) || (abort_mask && abort_mask[r]) || (P > max_pages);
+        int i;
+        for (i = 0; i < P && !dead; ++i) {
+            int32_t page = page_table[(int64_t)r * max_pages + i];
+            if (page < 0 || page >= num_pages)
+                dead = 1;
+        }
+        for (h = 0; h < Hq; ++h) {
+            int hk = h / G;
+            double *o = out + ((int64_t)r * Hq + h) * D;
+            const uint16_t *qr = q + ((int64_t)r * Hq + h) * D;
+            double m = -INFINITY, l = 0.0;
+            if (dead) {
+                for (d = 0; d < D; ++d) o[d] = 0.0;
+                lse[(int64_t)r * Hq + h] = -INFINITY;
+                continue;
+            }
+            for (j = 0; j < L; ++j) {
+                int64_t page = page_table[(int64_t)r * max_pages + j / ps];
+                double acc = 0.0;
+                for (d = 0; d < D; ++d) {
+                    double kv = load_k(k_pool, is_fp8, k_index(page, hk, j % ps, d, Hkv, ps, D), k_scale);
+                    acc += (double)bf16_bits_to_float(qr[d]) * kv;
+                }
+                scores[j] = acc * sm_scale;
+                if (scores[j] > m) m = scores[j];
+            }
+            for (d = 0; d < D; ++d) o[d] = 0.0;
+            for (j = 0; j < L; ++j) {
+                int64_t page = page_table[(int64_t)r * max_pages + j / ps];
+                double p = exp(scores[j] - m);
+                l += p;
+                for (d = 0; d < D; ++d)
+                    o[d] += p * load_k(v_pool, is_fp8, v_index(page, hk, j % ps, d, Hkv, ps, D), v_scale);
+            }
+            for (d = 0; d < D; ++d) o[d] /= l;
+            lse[(int64_t)r * Hq + h] = m + log(l);
+        }
+    }
+}
+
+/*
+ * Textbook dense attention for one query vector, written without paging:
+ * softmax(q K^T * sm_scale) V with K, V given densely as [L][D] doubles.
+ */
+void orc_dense_attention(const double *q, const double *K, const double *V, int L, int D,
+                         double sm_scale, double *scores, double *out, double *lse)
+{
+    int j, d;
+    double m = -INFINITY, z = 0.0;
+    for (j = 0; j < L; ++j) {
+        double s = 0.0;
+        for (d = 0; d < D; ++d) s += q[d] * K[(int64_t)j * D + d];
+        scores[j] = s * sm_scale;
+        m = fmax(m, scores[j]);
+    }
+    for (j = 0; j < L; ++j) {
+        scores[j] = exp(scores[j] - m);
+        z += scores[j];
+    }
+    for (d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (j = 0; j < L; ++j) acc += scores[j] / z * V[(int64_t)j * D + d];
+        out[d] = acc;
+    }
+    *lse = m + log(z);
+}
