@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 paged-KV decode-pool hot path on GB300.
+
+One step = one decode step of one layer over one batch: quantise-on-append of
+every request's new K/V token into its page, the separate batched page-tag
+check, and split-KV decode attention over the e4m3 cache (all of it in
+libfp8kv's kernels).  The BF16-cache variant of the same step runs on the
+identical values for comparison.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload b32_8k]
+  python bench.py --impl reference ...     # the CPU oracle, timed on host cores
+
+Multi-GPU (torchrun): every rank runs an independent replica (its own requests
+and pool); nothing on the data path is exchanged, only the timing is reduced.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = ("decode-attention tokens/s and achieved HBM GB/s (% of GB300 peak), FP8 vs BF16 KV")
+UNIT = "tokens/s"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only)
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the method must move per step)
+# ---------------------------------------------------------------------------
+def attention_bytes(wl, step: int, fp8: bool) -> int:
+    """KV bytes of every context token, page-table entries, queries and outputs."""
+    lens = wl.seq_lens_after(step).astype(np.int64)
+    b = 1 if fp8 else 2
+    kv = int(lens.sum()) * 2 * wl.Hkv * wl.D * b
+    pages = int((-(-lens // wl.page_size)).sum())
+    table = pages * 4
+    q = wl.B * wl.Hq * wl.D * 2
+    out = wl.B * wl.Hq * (wl.D + 1) * 4
+    return kv + table + q + out
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def read_profile_traffic(workload: str):
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_segment_problem(wl, r: int, h: int, step: int):
+    """One (request, kv head) segment as a compact single-head-group problem for
+    the oracle: that request's pages with only kv head h, renumbered 0..P-1."""
+    import oracle
+    L = int(wl.seq_lens_after(step)[r])
+    ps, D, G = wl.page_size, wl.D, wl.G
+    P = -(-L // ps)
+    a, b = int(wl.cu_prompt[r]), int(wl.cu_prompt[r + 1])
+    kp = np.full(P * ps * D, 0x7F, np.uint8)
+    vp = np.full(P * ps * D, 0x7F, np.uint8)
+    pt = np.arange(P, dtype=np.int32)[None, :]
+    k = np.ascontiguousarray(wl.k_prompt[a:b, h:h + 1])
+    v = np.ascontiguousarray(wl.v_prompt[a:b, h:h + 1])
+    oracle.kv_prefill(k, v, np.array([0, b - a], np.int32), kp, vp, wl.k_scale, wl.v_scale, pt,
+                      None, None, None, fp8=True, Hkv=1, D=D, page_size=ps, num_pages=P)
+    kn, vn = wl.step_tokens(step)
+    q = np.ascontiguousarray(wl.step_query(step)[r:r + 1, h * G:(h + 1) * G])
+    return dict(kn=np.ascontiguousarray(kn[r:r + 1, h:h + 1]), vn=np.ascontiguousarray(vn[r:r + 1, h:h + 1]),
+                kp=kp, vp=vp, pt=pt, lens=np.array([L], np.int32), q=q, P=P,
+                tags=np.zeros(P, np.uint32), exp=np.zeros((1, P), np.uint32))
+
+
+def oracle_segment_step(wl, prob) -> None:
+    """The oracle's decode step on one segment: append, tag check, fp64 attention."""
+    import oracle
+    ps = wl.page_size
+    oracle.kv_append(prob["kn"], prob["vn"], prob["kp"], prob["vp"], wl.k_scale, wl.v_scale,
+                     prob["pt"], prob["lens"], prob["tags"], prob["exp"], None, fp8=True, Hkv=1,
+                     D=wl.D, page_size=ps, num_pages=prob["P"])
+    mask, _ = oracle.page_tags_validate(prob["pt"], prob["exp"], prob["lens"], prob["tags"],
+                                        prob["P"], ps)
+    oracle.paged_attention(prob["q"], prob["kp"], prob["vp"], prob["pt"], prob["lens"], fp8=True,
+                           k_scale=wl.k_scale, v_scale=wl.v_scale, abort_mask=mask,
+                           sm_scale=wl.sm_scale, Hkv=1, page_size=ps, num_pages=prob["P"])
+
+
+def cpu_baseline(wl, budget_s: float = 12.0):
+    """Oracle throughput on a bounded sample: whole (request, kv head) segments
+    until ~budget_s of single-thread CPU work; one segment is 1/Hkv token."""
+    import oracle
+    oracle.build()
+    g = np.random.default_rng(0)
+    done, t_total, n = 0, 0.0, 0
+    while t_total < budget_s and n < wl.B * wl.Hkv:
+        r, h = int(g.integers(0, wl.B)), int(g.integers(0, wl.Hkv))
+        prob = oracle_segment_problem(wl, r, h, 0)
+        t0 = time.perf_counter()
+        oracle_segment_step(wl, prob)
+        t_total += time.perf_counter() - t0
+        done += 1
+        n += 1
+    tokens = done / wl.Hkv
+    return {"value": tokens / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} (request, kv head) segments of {wl.name} (append + tag check + fp64 "
+                      f"attention each, single thread, {t_total:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    from workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]()
+    g = np.random.default_rng(1)
+    probs = [oracle_segment_problem(wl, int(g.integers(0, wl.B)), int(g.integers(0, wl.Hkv)), 0)
+             for _ in range(4)]
+    for i in range(args.warmup):
+        oracle_segment_step(wl, probs[i % len(probs)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_segment_step(wl, probs[i % len(probs)])
+    dt = time.perf_counter() - t0
+    tokens = args.steps / wl.Hkv
+    value = tokens / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"each step: one (request, kv head) segment of {wl.name} "
+                                       "(append + tag check + fp64 attention), single thread"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl):
+    return {"workload": f"{wl.name}: B={wl.B}, Hq={wl.Hq}, Hkv={wl.Hkv}, D={wl.D}, "
+                        f"page_size={wl.page_size}, contexts {int(wl.seq_lens_after(0).min())}.."
+                        f"{int(wl.seq_lens_after(0).max())}, pool {wl.num_pages} pages",
+            "batch": wl.B, "layers": 1, "step": "append + page-tag validate + split-KV attention",
+            "l2": "inputs larger than L2 (KV pool > 129 MB)"}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def time_steps(pool, steps: int, warmup: int, validate: bool = True):
+    """Device time of `steps` decode steps; also the attention and validation kernels' own
+    event times (events recorded between launches on the launching stream)."""
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        pool.step(validate=validate)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(s)
+    for i in range(steps):
+        ev[i][0].record(s)
+        pool.append()
+        ev[i][1].record(s)
+        if validate:
+            pool.validate()
+        ev[i][2].record(s)
+        pool.attend(use_mask=validate)
+        ev[i][3].record(s)
+    end.record(s)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    attn = [e[2].elapsed_time(e[3]) for e in ev]
+    val = [e[1].elapsed_time(e[2]) for e in ev]
+    app = [e[0].elapsed_time(e[1]) for e in ev]
+    return total_ms, statistics.mean(attn), statistics.mean(val), statistics.mean(app)
+
+
+def time_e2e(pool, steps: int, warmup: int):
+    """Same step through the public API with host buffers: pinned H2D of the step's
+    inputs (q, new K/V rows, context lengths), the step, D2H of out/lse/abort mask."""
+    wl = pool.wl
+    s = torch.cuda.current_stream()
+    h_q = pool.q.cpu().pin_memory()
+    h_k = pool.k_new.cpu().pin_memory()
+    h_v = pool.v_new.cpu().pin_memory()
+    h_len = pool.seq_lens.cpu().pin_memory()
+    h_out = torch.empty_like(pool.out, device="cpu").pin_memory()
+    h_lse = torch.empty_like(pool.lse, device="cpu").pin_memory()
+    h_mask = torch.empty_like(pool.abort_mask, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_len))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_mask))
+
+    def one():
+        pool.q.copy_(h_q, non_blocking=True)
+        pool.k_new.copy_(h_k, non_blocking=True)
+        pool.v_new.copy_(h_v, non_blocking=True)
+        pool.seq_lens.copy_(h_len, non_blocking=True)
+        pool.step(validate=True)
+        h_out.copy_(pool.out, non_blocking=True)
+        h_lse.copy_(pool.lse, non_blocking=True)
+        h_mask.copy_(pool.abort_mask, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(steps):
+        one()
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="b32_8k")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import fp8_paged_kv_gb300 as fpk
+    from fp8_paged_kv_gb300 import build as fbuild
+    from fp8_paged_kv_gb300.pool import DecodePool
+    from workloads import WORKLOADS
+
+    if rank == 0 or world == 1:
+        fbuild.build()
+    barrier(world)
+    fpk.load_library()
+    wl = WORKLOADS[args.workload](seed=100 + rank) if world > 1 else WORKLOADS[args.workload]()
+
+    # ---------------- FP8 cache: the measured path
+    pool = DecodePool(wl, fp8=True, device=torch.device("cuda", torch.cuda.current_device()))
+    pool.prefill()
+    pool.set_step(0)
+    pool.step()
+    torch.cuda.synchronize()
+    live = int(wl.B - int(pool.abort_count.item()))
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        total_ms, attn_ms, val_ms, app_ms = time_steps(pool, args.steps, args.warmup)
+    barrier(world)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    value = live * world / (ms_step * 1e-3)
+
+    # validation overhead: the same step with the no-op tracker
+    noval_ms, _, _, _ = time_steps(pool, max(args.steps // 4, 20), 3, validate=False)
+    noval_step = noval_ms / max(args.steps // 4, 20)
+    status = fpk.fpk_decode_status(pool.workspace)
+
+    e2e_ms, h2d, d2h = time_e2e(pool, max(args.steps // 4, 20), 3)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+
+    abytes = attention_bytes(wl, 0, True)
+    peak, peak_kind = measured_peaks()
+    achieved = abytes / (attn_ms * 1e-3) / 1e9
+    # attention-only throughput and GB/s
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache; f16 MMA, fp32 softmax",
+        "data": "synthetic", "config": workload_config(wl),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": read_profile_traffic(wl.name),
+                     "kernel": "paged_decode attention (split-KV, FP8)",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "fp8": {"attn_us": attn_ms * 1e3, "validate_us": val_ms * 1e3, "append_us": app_ms * 1e3,
+                "attn_tokens_per_s": live * world / (attn_ms * 1e-3),
+                "attn_gbs": achieved, "step_us_without_validation": noval_step * 1e3,
+                "validation_overhead_pct": 100.0 * (ms_step - noval_step) / noval_step,
+                "algorithmic_bytes_per_attention": abytes, "status_word": status},
+        "gpu_launches": None, "clocks": clk.summary(),
+        "e2e": {"value": live * world / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+    }
+    launches_per_step = 3  # append, validate, attention (the combine is inside the attention kernel)
+    if args.steps:
+        out["gpu_launches"] = launches_per_step * args.steps
+    del pool
+    torch.cuda.empty_cache()
+
+    # ---------------- BF16 cache on identical values
+    if not args.no_bf16:
+        p16 = DecodePool(wl, fp8=False, device=torch.device("cuda", torch.cuda.current_device()))
+        p16.prefill()
+        p16.set_step(0)
+        n16 = max(args.steps // 4, 20)
+        t16, a16, v16, _ = time_steps(p16, n16, args.warmup)
+        b16 = attention_bytes(wl, 0, False)
+        out["bf16"] = {"value": live * world / (t16 / n16 * 1e-3), "ms_per_step": t16 / n16,
+                       "attn_us": a16 * 1e3, "attn_gbs": b16 / (a16 * 1e-3) / 1e9,
+                       "attn_frac": b16 / (a16 * 1e-3) / 1e9 / peak,
+                       "fp8_over_bf16_step": (t16 / n16) / ms_step}
+        del p16
+        torch.cuda.empty_cache()
+
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,45 @@
+// api.cu -- library-wide entry points and host helpers of libfp8kv.
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace fpk {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+}  // namespace
+
+int device_sm_count(int device) {
+  if (device < 0 || device >= kMaxDevices) return 0;
+  int v = g_sm_count[device].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+  g_sm_count[device].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Status after a launch: FPK_ECUDA if the launch reported an error.  The error
+// is peeked, not cleared, so that the caller's own checks still see it.
+int checked_launch_status() {
+  return cudaPeekAtLastError() == cudaSuccess ? FPK_OK : FPK_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace fpk
+
+extern "C" int fpk_version(void) { return 100; }
+
+extern "C" const char* fpk_status_str(int status) {
+  switch (status) {
+    case FPK_OK: return "ok";
+    case FPK_EINVAL: return "invalid argument (null pointer, negative size or Hq % Hkv != 0)";
+    case FPK_EUNSUPPORTED: return "unsupported size (D, page_size or group size)";
+    case FPK_ENOSPC: return "workspace too small";
+    case FPK_ECUDA: return "CUDA launch failed";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,811 @@
+// decode_attn.cu -- split-KV paged decode attention over the FP8 e4m3 (or the
+// BF16 comparison) cache, dequantising on read, plus the cross-split combine.
+//
+// The Cloudflare Kimi decode pool reads an FP8 e4m3 KV cache and the attention
+// kernel converts the values as it reads them ("Perche le cache piu piccole di
+// Cloudflare battono la velocita pura", remio.ai); pages are reusable physical
+// blocks reached through a per-sequence table and requests that failed the tag
+// check read nothing ("La sicurezza della cache KV condivisa...").  The pages
+// give no kernel design; this one is built for GB300:
+//
+// * Work split.  All (request, kv head) segments are laid end to end as a
+//   list of 16-token tiles; the grid's W CTAs take equal contiguous ranges of
+//   it (one wave with the automatic W), so variable context lengths cost no
+//   tail.  A CTA finds its start with a block scan over seq_lens.
+// * Data movement.  Warp 0 is a producer: it reads page ids 32 at a time and
+//   one lane issues cp.async.bulk (TMA) copies of each tile's K block
+//   [16 tok][128] and V block [128][16 tok] -- both contiguous in the pool
+//   layout -- into a ring of shared-memory stages completing on mbarriers,
+//   with an L2 evict-first hint.  Page ids outside the pool are never
+//   dereferenced.
+// * Math.  Consumer warps take ring stages round-robin.  With the GQA group on
+//   the N side of the tensor-core tile, S^T = K Q^T and O^T = V^T P^T are
+//   m16n8k16 MMAs; e4m3 codes convert exactly to f16 in registers (the query
+//   gets a per-head power-of-two prescale into f16 range), P is transposed
+//   from accumulator to operand layout with movmatrix, softmax is online in
+//   the log2 domain with warp-shuffle reductions.  The dims of each 16-wide
+//   k-step and the tokens of each tile are visited in a fixed permuted order
+//   (the same on both operands), so every operand fragment is a contiguous
+//   4-byte run of shared memory.
+// * Merge.  At the end of each segment piece the consumer warps merge their
+//   (m, l, O) in shared memory; a CTA that owns a whole segment writes the
+//   final output, otherwise it writes a partial and takes an arrival ticket;
+//   the warp that completes a segment's count merges its partials by
+//   log-sum-exp (one launch per call; nothing ever waits on another CTA).
+// * Safety.  Every wait is bounded (status word in the workspace); no barrier
+//   without a timeout is used after the prologue.
+#include <atomic>
+
+#include "common.cuh"
+
+namespace fpk {
+namespace {
+
+constexpr int kTile = 16;        // tokens per tile
+constexpr int kDim = 128;        // head dimension
+constexpr int kGroupMax = 8;     // query heads per kv head (N of the MMA tile)
+constexpr int kMergeStride = 132;  // floats per head row of the merge buffer
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <bool kFp8>
+struct Cfg {
+  static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kBlockBytes = kTile * kDim * kElem;  // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kBlockBytes;
+  static constexpr int kStages = kFp8 ? 16 : 8;
+  // Within a segment piece consumer warp c takes tiles c, c+4, ...; with
+  // kStages a multiple of the warp count, the previous round of a stage was
+  // consumed by the same warp, so no warp ever waits on a stage's mbarrier
+  // while its previous phase is still pending (the parity test would alias
+  // two phases back).  Across pieces the merge barrier gives the same order.
+  static_assert(kStages % kConsumerWarps == 0, "ring stages must be a multiple of the consumer warps");
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kMergeBytes = kConsumerWarps * kGroupMax * kMergeStride * 4;
+  static constexpr int kMlBytes = kConsumerWarps * kGroupMax * 4 * 2 + kConsumerWarps * 4;
+  static constexpr int kBarBytes = (2 * kStages + 2) * 8;
+  static constexpr int kSmemBytes = kRingBytes + kMergeBytes + kMlBytes + kBarBytes + kStages * 4 + 64;
+};
+
+struct AttnArgs {
+  const uint16_t* q;
+  const uint8_t* k_pool;
+  const uint8_t* v_pool;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const uint8_t* abort_mask;
+  float* out;
+  float* lse;
+  uint32_t* status;
+  int* seg_count;  // per-segment arrival tickets, zero between calls
+  float2* part_ml;
+  float* part_o;
+  int B, Hq, Hkv, G, page_size, num_pages, max_pages, W;
+  float sm_scale_log2;
+};
+
+struct Piece {
+  int r, h, t0, t1, n;
+  int64_t x0;  // global tile index of tile t0
+};
+
+struct Cursor {
+  int r, h, t, n;
+  int64_t x, remaining;
+};
+
+__device__ __forceinline__ int tiles_of(const AttnArgs& a, int r) {
+  return tiles_of_request(a.seq_lens, a.abort_mask, r, a.max_pages, a.page_size);
+}
+
+__device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, Piece& p) {
+  if (c.remaining <= 0) return false;
+  const int64_t left = c.n - c.t;
+  const int take = static_cast<int>(left < c.remaining ? left : c.remaining);
+  p.r = c.r;
+  p.h = c.h;
+  p.t0 = c.t;
+  p.t1 = c.t + take;
+  p.n = c.n;
+  p.x0 = c.x;
+  c.remaining -= take;
+  c.x += take;
+  c.t += take;
+  if (c.remaining > 0 && c.t == c.n) {
+    c.t = 0;
+    if (++c.h == a.Hkv) {
+      c.h = 0;
+      do {
+        ++c.r;
+        c.n = c.r < a.B ? tiles_of(a, c.r) : 1;
+      } while (c.n == 0);
+      if (c.r >= a.B) c.remaining = 0;  // unreachable with consistent inputs
+    }
+  }
+  return true;
+}
+
+// Worker w owns global tiles [floor(w T / W), floor((w+1) T / W)); the owner
+// of tile x is floor(((x + 1) W - 1) / T).  With W > T some workers own none.
+__device__ __forceinline__ int worker_of(int64_t x, int64_t T, int W) {
+  return static_cast<int>(((x + 1) * W - 1) / T);
+}
+// First worker after k that owns a tile: the owner of tile floor((k+1) T / W).
+__device__ __forceinline__ int next_worker(int k, int64_t T, int W) {
+  return worker_of(static_cast<int64_t>(k + 1) * T / W, T, W);
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Token (row of the tile) that fragment row i stands for: rows 2t, 2t+1,
+// 2t+8, 2t+9 map to tokens 4t..4t+3, so each lane's V operand is one
+// contiguous 4-token run.
+__device__ __forceinline__ int token_of_row(int i) {
+  return 4 * ((i & 7) >> 1) + (i & 1) + 2 * (i >> 3);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const AttnArgs a) {
+  using C = Cfg<kFp8>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* ring = smem;
+  float* s_o = reinterpret_cast<float*>(smem + C::kRingBytes);
+  float* s_m = s_o + kConsumerWarps * kGroupMax * kMergeStride;
+  float* s_l = s_m + kConsumerWarps * kGroupMax;
+  int* s_wfault = reinterpret_cast<int*>(s_l + kConsumerWarps * kGroupMax);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kMergeBytes + C::kMlBytes);
+  int* s_stage_fault = reinterpret_cast<int*>(bars + 2 * C::kStages + 2);
+
+  __shared__ int64_t s_warp_sum[kThreads / 32];
+  __shared__ int64_t s_total;
+  __shared__ int s_start[4];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int w = blockIdx.x;
+  const unsigned kFull = 0xffffffffu;
+
+  // ---- prologue: total tiles and this CTA's start (block scan over requests)
+  const int chunk = (a.B + kThreads - 1) / kThreads;
+  const int rb = tid * chunk;
+  const int re = min(a.B, rb + chunk);
+  int64_t mine = 0;
+  for (int r = rb; r < re; ++r) mine += tiles_of(a, r);
+  int64_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_warp_sum[warp] = incl;
+  if (tid == 0) {
+    s_start[0] = -1;
+  }
+  __syncthreads();
+  int64_t before = 0, total = 0;
+#pragma unroll
+  for (int i = 0; i < kThreads / 32; ++i) {
+    if (i < warp) before += s_warp_sum[i];
+    total += s_warp_sum[i];
+  }
+  const int64_t excl = before + incl - mine;
+  const int64_t T = total * a.Hkv;
+  const int64_t b0 = static_cast<int64_t>(w) * T / a.W;
+  const int64_t b1 = static_cast<int64_t>(w + 1) * T / a.W;
+  // requests that read nothing (empty, aborted, over-long) get out = 0 and
+  // lse = -inf; the CTAs share this round-robin
+  for (int r = w; r < a.B; r += a.W) {
+    if (tiles_of(a, r) == 0) {
+      float* orow = a.out + static_cast<int64_t>(r) * a.Hq * kDim;
+      for (int i = tid; i < a.Hq * kDim; i += kThreads) orow[i] = 0.f;
+      if (a.lse != nullptr)
+        for (int i = tid; i < a.Hq; i += kThreads) a.lse[static_cast<int64_t>(r) * a.Hq + i] = -INFINITY;
+    }
+  }
+  if (b0 >= b1) return;  // uniform over the CTA: empty range
+  if (mine > 0 && b0 >= excl * a.Hkv && b0 < (excl + mine) * a.Hkv) {
+    int64_t base = excl * a.Hkv;
+    for (int r = rb; r < re; ++r) {
+      const int n = tiles_of(a, r);
+      const int64_t span = static_cast<int64_t>(n) * a.Hkv;
+      if (b0 < base + span) {
+        const int64_t off = b0 - base;
+        s_start[0] = r;
+        s_start[1] = static_cast<int>(off / n);
+        s_start[2] = static_cast<int>(off % n);
+        s_start[3] = n;
+        break;
+      }
+      base += span;
+    }
+  }
+  if (tid == 0) s_total = T;
+  // barriers
+  const uint32_t full0 = smem_addr(bars);
+  const uint32_t empty0 = full0 + 8 * C::kStages;
+  const uint32_t merge_full = full0 + 16 * C::kStages;
+  const uint32_t merge_free = merge_full + 8;
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(merge_full, kConsumerWarps);
+    mbar_init(merge_free, kConsumerWarps);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (s_start[0] < 0) {  // inconsistent inputs (cannot happen): nothing to do
+    if (tid == 0) atomicOr(a.status, kStatusBadStart);
+    return;
+  }
+  Cursor start;
+  start.r = s_start[0];
+  start.h = s_start[1];
+  start.t = s_start[2];
+  start.n = s_start[3];
+  start.x = b0;
+  start.remaining = b1 - b0;
+  const int tpp = a.page_size >> 4;  // tiles per page
+
+  if (warp == 0) {
+    // ======================= producer warp =======================
+    const uint64_t pol = l2_policy_evict_first();
+    Cursor cur = start;
+    Piece p;
+    uint32_t j = 0;
+    bool ok = true;
+    while (ok && next_piece(cur, a, p)) {
+      const int32_t* ptrow = a.page_table + static_cast<int64_t>(p.r) * a.max_pages;
+      for (int t = p.t0; t < p.t1 && ok; t += 32) {
+        const int cnt = min(32, p.t1 - t);
+        int pid = 0;
+        if (lane < cnt) pid = __ldg(ptrow + (t + lane) / tpp);
+        for (int i = 0; i < cnt; ++i) {
+          const int page = __shfl_sync(kFull, pid, i);
+          const uint32_t stage = j % C::kStages;
+          const uint32_t round = j / C::kStages;
+          if (lane == 0) {
+            if (round > 0) ok = mbar_wait(empty0 + 8 * stage, (round - 1) & 1, a.status);
+            if (ok) {
+              const uint32_t fb = full0 + 8 * stage;
+              if (page >= 0 && page < a.num_pages) {
+                const int sub = (t + i) % tpp;
+                const int64_t blk = (static_cast<int64_t>(page) * a.Hkv + p.h) * tpp + sub;
+                s_stage_fault[stage] = 0;
+                mbar_arrive_expect_tx(fb, C::kStageBytes);
+                const uint32_t dst = smem_addr(ring + stage * C::kStageBytes);
+                bulk_g2s(dst, a.k_pool + blk * C::kBlockBytes, C::kBlockBytes, fb, pol);
+                bulk_g2s(dst + C::kBlockBytes, a.v_pool + blk * C::kBlockBytes, C::kBlockBytes, fb, pol);
+              } else {
+                s_stage_fault[stage] = 1;
+                mbar_arrive(fb);
+              }
+            }
+          }
+          ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          ++j;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // give in-flight copies (bounded) time to land before the CTA exits
+      for (uint32_t s = 0; s < C::kStages && s < j; ++s) {
+        const uint32_t issued = (j - 1 - s) / C::kStages + 1;
+        mbar_wait(full0 + 8 * s, (issued - 1) & 1, a.status);
+      }
+    }
+    return;
+  }
+
+  // ======================= consumer warps =======================
+  const int c = warp - 1;
+  const int g = lane >> 2;   // MMA group id: A row / B column
+  const int t4 = lane & 3;   // thread in group
+  const int rowA = token_of_row(g);  // token of fragment row g (row g+8 is rowA + 2)
+  const float kscale = kFp8 ? __ldg(a.k_scale) : 1.f;
+  const float vscale = kFp8 ? __ldg(a.v_scale) : 1.f;
+  const float vmul = kFp8 ? vscale : 1.f;
+  Cursor cur = start;
+  Piece p;
+  uint32_t jbase = 0;
+  uint32_t piece_idx = 0;
+  bool ok = true;
+  const float kNegInf = -INFINITY;
+
+  while (ok && next_piece(cur, a, p)) {
+    const int ntiles = p.t1 - p.t0;
+    const int L = __ldg(a.seq_lens + p.r);
+    // ---- query fragments (B operand of S^T = K Q^T), heads of this kv group
+    uint32_t qf[8][2];
+    float mult_own = 0.f;
+    {
+      const bool has = g < a.G;
+      const uint16_t* qrow = a.q + (static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + (has ? g : 0)) * kDim;
+      if (kFp8) {
+        float v[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint4 raw = make_uint4(0, 0, 0, 0);
+            if (has) raw = __ldg(reinterpret_cast<const uint4*>(qrow + 64 * cc + 16 * t4 + 8 * hh));
+            const uint16_t* e = reinterpret_cast<const uint16_t*>(&raw);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[16 * cc + 8 * hh + k] = bf16_bits_to_float(e[k]);
+          }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+        // power-of-two prescale taking the head's largest |q| into [2^14, 2^15)
+        int e2 = 0;
+        if (amax > 0.f && isfinite(amax)) e2 = min(max(14 - ilogbf(amax), -126), 126);
+        const float sc = __int_as_float((127 + e2) << 23);
+        const float isc = __int_as_float((127 - e2) << 23);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int o = 16 * (kk >> 2) + 4 * (kk & 3);
+          qf[kk][0] = pack_f16x2(v[o] * sc, v[o + 1] * sc);
+          qf[kk][1] = pack_f16x2(v[o + 2] * sc, v[o + 3] * sc);
+        }
+        mult_own = has ? kscale * a.sm_scale_log2 * isc : 0.f;
+      } else {
+        uint4 raw[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          raw[cc] = make_uint4(0, 0, 0, 0);
+          if (has) raw[cc] = __ldg(reinterpret_cast<const uint4*>(qrow + 32 * cc + 8 * t4));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qf[kk][0] = word_of(raw[kk >> 1], 2 * (kk & 1));
+          qf[kk][1] = word_of(raw[kk >> 1], 2 * (kk & 1) + 1);
+        }
+        mult_own = has ? a.sm_scale_log2 : 0.f;
+      }
+    }
+    // score multipliers of the two heads (2*t4, 2*t4+1) whose columns this lane holds
+    const float mult0 = __shfl_sync(kFull, mult_own, 8 * t4);
+    const float mult1 = __shfl_sync(kFull, mult_own, 8 * t4 + 4);
+
+    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    int fault = 0;
+
+    for (int i = c; i < ntiles; i += kConsumerWarps) {
+      const uint32_t j = jbase + i;
+      const uint32_t stage = j % C::kStages;
+      const uint32_t round = j / C::kStages;
+      const bool got = mbar_wait(full0 + 8 * stage, round & 1, a.status);
+      if (!__all_sync(kFull, got)) {
+        ok = false;
+        break;
+      }
+      if (s_stage_fault[stage]) {
+        fault = 1;
+      } else {
+        const uint8_t* Ks = ring + stage * C::kStageBytes;
+        const uint8_t* Vs = Ks + C::kBlockBytes;
+        const int nvalid = min(kTile, L - (p.t0 + i) * kTile);
+        // ---- S^T = K Q^T  (rows: tokens, cols: heads)
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        if (kFp8) {
+          const uint4 ka0 = lds128(Ks + rowA * kDim + 16 * t4);
+          const uint4 ka1 = lds128(Ks + rowA * kDim + 64 + 16 * t4);
+          const uint4 kb0 = lds128(Ks + (rowA + 2) * kDim + 16 * t4);
+          const uint4 kb1 = lds128(Ks + (rowA + 2) * kDim + 64 + 16 * t4);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t wa = word_of(kk < 4 ? ka0 : ka1, kk & 3);
+            const uint32_t wb = word_of(kk < 4 ? kb0 : kb1, kk & 3);
+            const uint32_t af[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(wa)),
+                                    e4m3x2_to_f16x2(static_cast<uint16_t>(wb)),
+                                    e4m3x2_to_f16x2(static_cast<uint16_t>(wa >> 16)),
+                                    e4m3x2_to_f16x2(static_cast<uint16_t>(wb >> 16))};
+            if (kk & 1) mma_f16(acc1, af, qf[kk][0], qf[kk][1]);
+            else mma_f16(acc0, af, qf[kk][0], qf[kk][1]);
+          }
+        } else {
+          uint4 ka[4], kb[4];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            ka[cc] = lds128(Ks + rowA * 2 * kDim + 64 * cc + 16 * t4);
+            kb[cc] = lds128(Ks + (rowA + 2) * 2 * kDim + 64 * cc + 16 * t4);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int wi = 2 * (kk & 1);
+            const uint32_t af[4] = {word_of(ka[kk >> 1], wi), word_of(kb[kk >> 1], wi),
+                                    word_of(ka[kk >> 1], wi + 1), word_of(kb[kk >> 1], wi + 1)};
+            if (kk & 1) mma_bf16(acc1, af, qf[kk][0], qf[kk][1]);
+            else mma_bf16(acc0, af, qf[kk][0], qf[kk][1]);
+          }
+        }
+        float s0 = (acc0[0] + acc1[0]) * mult0;
+        float s1 = (acc0[1] + acc1[1]) * mult1;
+        float s2 = (acc0[2] + acc1[2]) * mult0;
+        float s3 = (acc0[3] + acc1[3]) * mult1;
+        if (nvalid < kTile) {
+          if (rowA >= nvalid) s0 = s1 = kNegInf;
+          if (rowA + 2 >= nvalid) s2 = s3 = kNegInf;
+        }
+        // ---- online softmax (log2 domain), per head over the tile's tokens
+        float tm0 = fmaxf(s0, s2), tm1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, off));
+          tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, off));
+        }
+        const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+        if (__any_sync(kFull, mn0 > m0 || mn1 > m1)) {
+          const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+          }
+          l0 *= al0;
+          l1 *= al1;
+          m0 = mn0;
+          m1 = mn1;
+        }
+        const float p0 = fast_exp2(s0 - m0), p1 = fast_exp2(s1 - m1);
+        const float p2 = fast_exp2(s2 - m0), p3 = fast_exp2(s3 - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        // ---- P^T as the B operand of O^T = V^T P^T
+        // (bf16 keeps only 8 significant bits, so the bf16 cache multiplies V by
+        // P = hi + lo, two bf16 parts; f16 P is exact enough for the FP8 cache)
+        const uint32_t pr0 = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+        const uint32_t pr1 = kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3);
+        const uint32_t pb0 = movmatrix_trans(pr0);
+        const uint32_t pb1 = movmatrix_trans(pr1);
+        uint32_t pl0 = 0, pl1 = 0;
+        if (!kFp8) {
+          pl0 = movmatrix_trans(pack_bf16x2(p0 - __uint_as_float(pr0 << 16),
+                                            p1 - __uint_as_float(pr0 & 0xffff0000u)));
+          pl1 = movmatrix_trans(pack_bf16x2(p2 - __uint_as_float(pr1 << 16),
+                                            p3 - __uint_as_float(pr1 & 0xffff0000u)));
+        }
+        // mask for V columns past the context (stale slots may hold NaN codes)
+        const int nv = nvalid - 4 * t4;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          if (kFp8) {
+            uint32_t va = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g) * 16 + 4 * t4);
+            uint32_t vb = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g + 8) * 16 + 4 * t4);
+            if (nv < 4) {
+              const uint32_t keep = nv <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nv)));
+              va &= keep;
+              vb &= keep;
+            }
+            const uint32_t af[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(va)),
+                                    e4m3x2_to_f16x2(static_cast<uint16_t>(vb)),
+                                    e4m3x2_to_f16x2(static_cast<uint16_t>(va >> 16)),
+                                    e4m3x2_to_f16x2(static_cast<uint16_t>(vb >> 16))};
+            mma_f16(o[mt], af, pb0, pb1);
+          } else {
+            uint2 va = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g) * 32 + 8 * t4);
+            uint2 vb = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g + 8) * 32 + 8 * t4);
+            if (nv < 4) {
+              const uint32_t k0 = nv <= 0 ? 0u : nv == 1 ? 0x0000ffffu : 0xffffffffu;
+              const uint32_t k1 = nv <= 2 ? 0u : nv == 3 ? 0x0000ffffu : 0xffffffffu;
+              va.x &= k0;
+              va.y &= k1;
+              vb.x &= k0;
+              vb.y &= k1;
+            }
+            const uint32_t af[4] = {va.x, vb.x, va.y, vb.y};
+            mma_bf16(o[mt], af, pb0, pb1);
+            mma_bf16(o[mt], af, pl0, pl1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+    }
+    jbase += ntiles;
+    if (!ok) break;
+
+    // ---- merge the consumer warps' (m, l, O) of this piece
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(kFull, l0, off);
+      l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+    fault = __any_sync(kFull, fault);
+    if (piece_idx > 0) {
+      const bool got = mbar_wait(merge_free, (piece_idx - 1) & 1, a.status);
+      if (!__all_sync(kFull, got)) break;
+    }
+    {
+      float* mo = s_o + c * kGroupMax * kMergeStride;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        mo[(2 * t4) * kMergeStride + 16 * mt + g] = o[mt][0];
+        mo[(2 * t4 + 1) * kMergeStride + 16 * mt + g] = o[mt][1];
+        mo[(2 * t4) * kMergeStride + 16 * mt + g + 8] = o[mt][2];
+        mo[(2 * t4 + 1) * kMergeStride + 16 * mt + g + 8] = o[mt][3];
+      }
+      if (g == 0) {
+        s_m[c * kGroupMax + 2 * t4] = m0;
+        s_m[c * kGroupMax + 2 * t4 + 1] = m1;
+        s_l[c * kGroupMax + 2 * t4] = l0;
+        s_l[c * kGroupMax + 2 * t4 + 1] = l1;
+      }
+      if (lane == 0) s_wfault[c] = fault;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(merge_full);
+    {
+      const bool got = mbar_wait(merge_full, piece_idx & 1, a.status);
+      if (!__all_sync(kFull, got)) break;
+    }
+    const int seg = p.r * a.Hkv + p.h;
+    const bool whole = p.t0 == 0 && p.t1 == p.n;
+    const int ct = c * 32 + lane;
+    int anyfault = 0;
+#pragma unroll
+    for (int k = 0; k < kConsumerWarps; ++k) anyfault |= s_wfault[k];
+    for (int idx = ct; idx < a.G * kDim; idx += kConsumerWarps * 32) {
+      const int hd = idx >> 7;
+      const int d = idx & (kDim - 1);
+      float M = kNegInf;
+#pragma unroll
+      for (int k = 0; k < kConsumerWarps; ++k) M = fmaxf(M, s_m[k * kGroupMax + hd]);
+      const bool dead = anyfault || M == kNegInf;
+      float wsum = 0.f, acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < kConsumerWarps; ++k) {
+        const float mk = s_m[k * kGroupMax + hd];
+        const float f = mk == kNegInf ? 0.f : fast_exp2(mk - M);
+        wsum += s_l[k * kGroupMax + hd] * f;
+        acc += s_o[(k * kGroupMax + hd) * kMergeStride + d] * f;
+      }
+      if (whole) {
+        const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
+        a.out[row * kDim + d] = dead ? 0.f : acc * vmul / wsum;
+        if (d == 0 && a.lse != nullptr) a.lse[row] = dead ? kNegInf : (M + __log2f(wsum)) * kLn2;
+      } else {
+        const int64_t slot = static_cast<int64_t>(seg) + w;
+        a.part_o[(slot * a.G + hd) * kDim + d] = acc * vmul;
+        if (d == 0) a.part_ml[slot * a.G + hd] = dead ? make_float2(kNegInf, -1.f) : make_float2(M, wsum);
+      }
+    }
+    if (!whole) {
+      // Arrival ticket per consumer warp: the warp that completes the count
+      // for this segment merges all its CTAs' partials (no waiting anywhere).
+      __threadfence();
+      __syncwarp();
+      const int64_t xseg = p.x0 - p.t0;  // global index of the segment's first tile
+      const int64_t T = s_total;
+      const int w0 = worker_of(xseg, T, a.W);
+      const int w1 = worker_of(xseg + p.n - 1, T, a.W);
+      // CTAs holding a piece of this segment: all of w0..w1 when every worker
+      // owns tiles (T >= W), else one per tile
+      const int contributors = T >= a.W ? w1 - w0 + 1 : p.n;
+      int last = 0;
+      if (lane == 0) last = atomicAdd(a.seg_count + seg, 1) == contributors * kConsumerWarps - 1;
+      last = __shfl_sync(kFull, last, 0);
+      if (last) {
+        __threadfence();
+        for (int hd = 0; hd < a.G; ++hd) {
+          float M = kNegInf;
+          bool dead = false;
+          for (int k = w0; k <= w1; k = next_worker(k, T, a.W)) {
+            const float2 ml = __ldcg(a.part_ml + (static_cast<int64_t>(seg) + k) * a.G + hd);
+            dead |= ml.y < 0.f;
+            M = fmaxf(M, ml.x);
+          }
+          dead |= M == kNegInf;
+          float wsum = 0.f, acc[kDim / 32];
+#pragma unroll
+          for (int e = 0; e < kDim / 32; ++e) acc[e] = 0.f;
+          for (int k = w0; k <= w1 && !dead; k = next_worker(k, T, a.W)) {
+            const int64_t slot = static_cast<int64_t>(seg) + k;
+            const float2 ml = __ldcg(a.part_ml + slot * a.G + hd);
+            const float f = ml.x == kNegInf ? 0.f : fast_exp2(ml.x - M);
+            wsum += ml.y * f;
+            const float* po = a.part_o + (slot * a.G + hd) * kDim;
+#pragma unroll
+            for (int e = 0; e < kDim / 32; ++e) acc[e] += __ldcg(po + lane + 32 * e) * f;
+          }
+          const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
+#pragma unroll
+          for (int e = 0; e < kDim / 32; ++e) a.out[row * kDim + lane + 32 * e] = dead ? 0.f : acc[e] / wsum;
+          if (lane == 0 && a.lse != nullptr) a.lse[row] = dead ? kNegInf : (M + __log2f(wsum)) * kLn2;
+        }
+        if (lane == 0) a.seg_count[seg] = 0;  // ready for the next call
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(merge_free);
+    ++piece_idx;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_auto_ctas[2][kMaxDevices];  // resident CTAs per SM, per variant
+
+template <bool kFp8>
+int prepare_kernel(int dev) {
+  std::atomic<int>& slot = g_auto_ctas[kFp8 ? 1 : 0][dev];
+  int v = slot.load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  auto kern = paged_decode_split_kernel<kFp8>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kFp8>::kSmemBytes) !=
+      cudaSuccess)
+    return -1;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Cfg<kFp8>::kSmemBytes) !=
+          cudaSuccess ||
+      per_sm <= 0)
+    return -1;
+  slot.store(per_sm, std::memory_order_relaxed);
+  return per_sm;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t seg_count, part_ml, part_o, total;
+};
+
+WsLayout layout(int64_t B, int64_t Hkv, int64_t G, int64_t W) {
+  WsLayout l;
+  const int64_t segs = B * Hkv;
+  const int64_t slots = segs + W;
+  l.seg_count = 256;
+  l.part_ml = l.seg_count + align256(static_cast<size_t>(segs) * sizeof(int));
+  l.part_o = l.part_ml + align256(static_cast<size_t>(slots * G) * sizeof(float2));
+  l.total = l.part_o + align256(static_cast<size_t>(slots * G * kDim) * sizeof(float));
+  return l;
+}
+
+int auto_workers(int dev) {
+  const int sms = device_sm_count(dev);
+  const int a8 = prepare_kernel<true>(dev);
+  const int a16 = prepare_kernel<false>(dev);
+  if (sms <= 0 || a8 <= 0 || a16 <= 0) return -1;
+  return sms * (a8 > a16 ? a8 : a16);
+}
+
+int check_attn_shapes(int B, int Hq, int Hkv, int D, int page_size, int num_pages, int max_pages,
+                      int num_splits) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 || max_pages < 0 ||
+      num_splits < 0)
+    return FPK_EINVAL;
+  if (Hq % Hkv != 0) return FPK_EINVAL;
+  const int G = Hq / Hkv;
+  if (D != kDim || G > kGroupMax || page_size % kTile != 0 || page_size > 256) return FPK_EUNSUPPORTED;
+  return FPK_OK;
+}
+
+template <bool kFp8>
+int attn_entry(const void* q, const void* k_pool, const void* v_pool, const float* k_scale,
+               const float* v_scale, const int32_t* page_table, int32_t max_pages,
+               const int32_t* seq_lens, const uint8_t* abort_mask, float* out, float* lse,
+               void* workspace, size_t workspace_bytes, int32_t num_splits, float sm_scale,
+               int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+               int32_t num_pages, void* stream) {
+  int st = check_attn_shapes(B, Hq, Hkv, D, page_size, num_pages, max_pages, num_splits);
+  if (st != FPK_OK) return st;
+  if (B == 0) return FPK_OK;
+  if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out || !workspace) return FPK_EINVAL;
+  if (kFp8 && (!k_scale || !v_scale)) return FPK_EINVAL;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FPK_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FPK_ECUDA;
+  if (prepare_kernel<kFp8>(dev) <= 0) return FPK_ECUDA;
+  int W = num_splits;
+  if (W == 0) {
+    W = device_sm_count(dev) * prepare_kernel<kFp8>(dev);
+    if (W <= 0) return FPK_ECUDA;
+  }
+  const int G = Hq / Hkv;
+  const WsLayout l = layout(B, Hkv, G, W);
+  if (workspace_bytes < l.total) return FPK_ENOSPC;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  AttnArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_pool = static_cast<const uint8_t*>(k_pool);
+  a.v_pool = static_cast<const uint8_t*>(v_pool);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.abort_mask = abort_mask;
+  a.out = out;
+  a.lse = lse;
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.seg_count = reinterpret_cast<int*>(ws + l.seg_count);
+  a.part_ml = reinterpret_cast<float2*>(ws + l.part_ml);
+  a.part_o = reinterpret_cast<float*>(ws + l.part_o);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = G;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
+  a.W = W;
+  a.sm_scale_log2 = sm_scale * kLog2e;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  paged_decode_split_kernel<kFp8><<<W, kThreads, Cfg<kFp8>::kSmemBytes, s>>>(a);
+  return checked_launch_status();
+}
+
+}  // namespace
+}  // namespace fpk
+
+extern "C" size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                             int32_t num_splits) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_splits < 0 || D != fpk::kDim) return 0;
+  int W = num_splits;
+  if (W == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fpk::kMaxDevices) return 0;
+    W = fpk::auto_workers(dev);
+    if (W <= 0) return 0;
+  }
+  return fpk::layout(B, Hkv, Hq / Hkv, W).total;
+}
+
+extern "C" int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                                         const float* k_scale, const float* v_scale,
+                                         const int32_t* page_table, int32_t max_pages,
+                                         const int32_t* seq_lens, const uint8_t* abort_mask,
+                                         float* out, float* lse, void* workspace,
+                                         size_t workspace_bytes, int32_t num_splits,
+                                         float sm_scale, int32_t B, int32_t Hq, int32_t Hkv,
+                                         int32_t D, int32_t page_size, int32_t num_pages,
+                                         void* stream) {
+  return fpk::attn_entry<true>(q, k_pool, v_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
+                               abort_mask, out, lse, workspace, workspace_bytes, num_splits,
+                               sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream);
+}
+
+extern "C" int fpk_paged_decode_attn_bf16(const void* q, const void* k_pool, const void* v_pool,
+                                          const int32_t* page_table, int32_t max_pages,
+                                          const int32_t* seq_lens, const uint8_t* abort_mask,
+                                          float* out, float* lse, void* workspace,
+                                          size_t workspace_bytes, int32_t num_splits,
+                                          float sm_scale, int32_t B, int32_t Hq, int32_t Hkv,
+                                          int32_t D, int32_t page_size, int32_t num_pages,
+                                          void* stream) {
+  return fpk::attn_entry<false>(q, k_pool, v_pool, nullptr, nullptr, page_table, max_pages, seq_lens,
+                                abort_mask, out, lse, workspace, workspace_bytes, num_splits,
+                                sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream);
+}
+
+extern "C" int fpk_decode_status(const void* workspace, int32_t* status, void* stream) {
+  if (!workspace || !status) return FPK_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FPK_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FPK_ECUDA;
+  return FPK_OK;
+}

@@ -1,0 +1,260 @@
+// kv_write.cu -- quantise-on-append and bulk prompt writes into the paged cache.
+//
+// The decode pool of the Cloudflare Kimi deployment keeps its KV cache as FP8
+// e4m3 in place of BF16 ("Cosa ha cambiato Cloudflare per Kimi e GLM",
+// remio.ai); requests write pages of the shared physical cache as well as
+// read them (iitog.ru summary, third technique).  Every token write is
+// guarded by its destination page's tag so that a stale mapping can never
+// overwrite a page another request now owns: the write is skipped and the
+// request is marked aborted.
+//
+// One thread handles 8 consecutive dims of one (token, kv head): a 16-byte
+// bf16 load per tensor, an 8-byte (fp8) or 16-byte (bf16) store into the
+// token-major K row, and 8 strided element stores into the V column block.
+#include "common.cuh"
+
+namespace fpk {
+namespace {
+
+struct WriteArgs {
+  const uint16_t* k_src;     // bf16 [rows][Hkv][D]
+  const uint16_t* v_src;
+  const int32_t* seq_lens;   // decode mode: position = seq_lens[r] - 1, row r
+  const int32_t* cu_seqlens; // prefill mode: row i of request r at position i - cu[r]
+  uint8_t* k_pool;
+  uint8_t* v_pool;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* page_table;
+  const uint32_t* live_tags;
+  const uint32_t* expected_tags;
+  uint8_t* abort_mask;
+  int64_t rows;
+  int B, Hkv, D, page_size, num_pages, max_pages;
+};
+
+__device__ __forceinline__ int request_of_row(const int32_t* cu, int B, int64_t row) {
+  // largest r with cu[r] <= row (cu non-decreasing, cu[0] = 0)
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(__ldg(cu + mid)) <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <bool kFp8, bool kPrefill>
+__global__ void __launch_bounds__(256) write_tokens_kernel(WriteArgs a) {
+  const int chunks = a.D >> 3;
+  const int64_t units = a.rows * a.Hkv * chunks;
+  const float ks = kFp8 ? __ldg(a.k_scale) : 1.f;
+  const float vs = kFp8 ? __ldg(a.v_scale) : 1.f;
+  for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(u % chunks);
+    const int h = static_cast<int>((u / chunks) % a.Hkv);
+    const int64_t row = u / (static_cast<int64_t>(chunks) * a.Hkv);
+    int r, pos;
+    if (kPrefill) {
+      r = request_of_row(a.cu_seqlens, a.B, row);
+      pos = static_cast<int>(row - __ldg(a.cu_seqlens + r));
+    } else {
+      r = static_cast<int>(row);
+      pos = __ldg(a.seq_lens + r) - 1;
+      if (pos < 0) continue;
+    }
+    const int pi = pos / a.page_size;
+    const int off = pos - pi * a.page_size;
+    bool ok = pi < a.max_pages;
+    int page = -1;
+    if (ok) {
+      page = __ldg(a.page_table + static_cast<int64_t>(r) * a.max_pages + pi);
+      ok = page >= 0 && page < a.num_pages;
+    }
+    if (ok && a.live_tags != nullptr && a.expected_tags != nullptr)
+      ok = __ldg(a.live_tags + page) ==
+           __ldg(a.expected_tags + static_cast<int64_t>(r) * a.max_pages + pi);
+    if (!ok) {
+      if (a.abort_mask != nullptr) a.abort_mask[r] = 1;
+      continue;
+    }
+    const int64_t src = (row * a.Hkv + h) * a.D + 8 * c;
+    const uint4 kraw = __ldg(reinterpret_cast<const uint4*>(a.k_src + src));
+    const uint4 vraw = __ldg(reinterpret_cast<const uint4*>(a.v_src + src));
+    const int64_t kdst = ((static_cast<int64_t>(page) * a.Hkv + h) * a.page_size + off) * a.D + 8 * c;
+    const int64_t vblk = ((static_cast<int64_t>(page) * a.Hkv + h) * (a.page_size >> 4) + (off >> 4)) *
+                         a.D * 16;
+    const int vcol = off & 15;
+    const uint16_t* kb = reinterpret_cast<const uint16_t*>(&kraw);
+    const uint16_t* vb = reinterpret_cast<const uint16_t*>(&vraw);
+    if (kFp8) {
+      uint32_t kw[2];
+      uint8_t vq[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float k0 = __fdiv_rn(bf16_bits_to_float(kb[2 * i]), ks);
+        const float k1 = __fdiv_rn(bf16_bits_to_float(kb[2 * i + 1]), ks);
+        const float v0 = __fdiv_rn(bf16_bits_to_float(vb[2 * i]), vs);
+        const float v1 = __fdiv_rn(bf16_bits_to_float(vb[2 * i + 1]), vs);
+        const uint16_t kp = __nv_cvt_float2_to_fp8x2(make_float2(k0, k1), __NV_SATFINITE, __NV_E4M3);
+        const uint16_t vp = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
+        if (i & 1) kw[i >> 1] |= static_cast<uint32_t>(kp) << 16; else kw[i >> 1] = kp;
+        vq[2 * i] = static_cast<uint8_t>(vp & 0xFF);
+        vq[2 * i + 1] = static_cast<uint8_t>(vp >> 8);
+      }
+      *reinterpret_cast<uint2*>(a.k_pool + kdst) = make_uint2(kw[0], kw[1]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a.v_pool[vblk + static_cast<int64_t>(8 * c + i) * 16 + vcol] = vq[i];
+    } else {
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.k_pool) + kdst) = kraw;
+      uint16_t* vpool = reinterpret_cast<uint16_t*>(a.v_pool);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) vpool[vblk + static_cast<int64_t>(8 * c + i) * 16 + vcol] = vb[i];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ x,
+                                                       const float* __restrict__ scale,
+                                                       uint8_t* __restrict__ out, int64_t n) {
+  const float s = __ldg(scale);
+  const int64_t pairs = n >> 1;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < pairs;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float a = __fdiv_rn(__ldg(x + 2 * i), s);
+    const float b = __fdiv_rn(__ldg(x + 2 * i + 1), s);
+    const uint16_t p = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    out[2 * i] = static_cast<uint8_t>(p & 0xFF);
+    out[2 * i + 1] = static_cast<uint8_t>(p >> 8);
+  }
+  if ((n & 1) && blockIdx.x == 0 && threadIdx.x == 0) {
+    const float a = __fdiv_rn(__ldg(x + n - 1), s);
+    const uint16_t p = __nv_cvt_float2_to_fp8x2(make_float2(a, 0.f), __NV_SATFINITE, __NV_E4M3);
+    out[n - 1] = static_cast<uint8_t>(p & 0xFF);
+  }
+}
+
+int check_shapes(int B, int Hkv, int D, int page_size, int num_pages, int max_pages) {
+  if (B < 0 || Hkv <= 0 || D <= 0 || page_size <= 0 || num_pages < 0 || max_pages < 0)
+    return FPK_EINVAL;
+  if (D != 128 || page_size % 16 != 0 || page_size > 256) return FPK_EUNSUPPORTED;
+  return FPK_OK;
+}
+
+int launch_write(const WriteArgs& a, bool fp8, bool prefill, cudaStream_t s) {
+  const int64_t units = a.rows * a.Hkv * (a.D >> 3);
+  if (units == 0) return FPK_OK;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int64_t want = (units + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(device_sm_count(dev) > 0 ? device_sm_count(dev) : 132) * 16;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  if (fp8) {
+    if (prefill) write_tokens_kernel<true, true><<<grid, 256, 0, s>>>(a);
+    else write_tokens_kernel<true, false><<<grid, 256, 0, s>>>(a);
+  } else {
+    if (prefill) write_tokens_kernel<false, true><<<grid, 256, 0, s>>>(a);
+    else write_tokens_kernel<false, false><<<grid, 256, 0, s>>>(a);
+  }
+  return checked_launch_status();
+}
+
+int write_entry(bool fp8, bool prefill, const void* k, const void* v, const int32_t* seq_lens,
+                const int32_t* cu, int64_t rows, void* k_pool, void* v_pool, const float* k_scale,
+                const float* v_scale, const int32_t* page_table, int32_t max_pages,
+                const uint32_t* live_tags, const uint32_t* expected_tags, uint8_t* abort_mask,
+                int32_t B, int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                void* stream) {
+  int st = check_shapes(B, Hkv, D, page_size, num_pages, max_pages);
+  if (st != FPK_OK) return st;
+  if (rows < 0) return FPK_EINVAL;
+  if (rows == 0 || B == 0) return FPK_OK;
+  if (!k || !v || !k_pool || !v_pool || !page_table || (prefill ? !cu : !seq_lens))
+    return FPK_EINVAL;
+  if (fp8 && (!k_scale || !v_scale)) return FPK_EINVAL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool)) return FPK_EINVAL;
+  WriteArgs a;
+  a.k_src = static_cast<const uint16_t*>(k);
+  a.v_src = static_cast<const uint16_t*>(v);
+  a.seq_lens = seq_lens;
+  a.cu_seqlens = cu;
+  a.k_pool = static_cast<uint8_t*>(k_pool);
+  a.v_pool = static_cast<uint8_t*>(v_pool);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.page_table = page_table;
+  a.live_tags = live_tags;
+  a.expected_tags = expected_tags;
+  a.abort_mask = abort_mask;
+  a.rows = rows;
+  a.B = B;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
+  return launch_write(a, fp8, prefill, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace fpk
+
+extern "C" int fpk_kv_append_fp8(const void* k_new, const void* v_new, uint8_t* k_pool,
+                                 uint8_t* v_pool, const float* k_scale, const float* v_scale,
+                                 const int32_t* page_table, int32_t max_pages,
+                                 const int32_t* seq_lens, const uint32_t* live_tags,
+                                 const uint32_t* expected_tags, uint8_t* abort_mask, int32_t B,
+                                 int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                                 void* stream) {
+  return fpk::write_entry(true, false, k_new, v_new, seq_lens, nullptr, B, k_pool, v_pool, k_scale,
+                          v_scale, page_table, max_pages, live_tags, expected_tags, abort_mask, B,
+                          Hkv, D, page_size, num_pages, stream);
+}
+
+extern "C" int fpk_kv_append_bf16(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                  const int32_t* page_table, int32_t max_pages,
+                                  const int32_t* seq_lens, const uint32_t* live_tags,
+                                  const uint32_t* expected_tags, uint8_t* abort_mask, int32_t B,
+                                  int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                                  void* stream) {
+  return fpk::write_entry(false, false, k_new, v_new, seq_lens, nullptr, B, k_pool, v_pool, nullptr,
+                          nullptr, page_table, max_pages, live_tags, expected_tags, abort_mask, B,
+                          Hkv, D, page_size, num_pages, stream);
+}
+
+extern "C" int fpk_kv_prefill_fp8(const void* k, const void* v, const int32_t* cu_seqlens,
+                                  int32_t n_tokens, uint8_t* k_pool, uint8_t* v_pool,
+                                  const float* k_scale, const float* v_scale,
+                                  const int32_t* page_table, int32_t max_pages,
+                                  const uint32_t* live_tags, const uint32_t* expected_tags,
+                                  uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
+                                  int32_t page_size, int32_t num_pages, void* stream) {
+  return fpk::write_entry(true, true, k, v, nullptr, cu_seqlens, n_tokens, k_pool, v_pool, k_scale,
+                          v_scale, page_table, max_pages, live_tags, expected_tags, abort_mask, B,
+                          Hkv, D, page_size, num_pages, stream);
+}
+
+extern "C" int fpk_kv_prefill_bf16(const void* k, const void* v, const int32_t* cu_seqlens,
+                                   int32_t n_tokens, void* k_pool, void* v_pool,
+                                   const int32_t* page_table, int32_t max_pages,
+                                   const uint32_t* live_tags, const uint32_t* expected_tags,
+                                   uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
+                                   int32_t page_size, int32_t num_pages, void* stream) {
+  return fpk::write_entry(false, true, k, v, nullptr, cu_seqlens, n_tokens, k_pool, v_pool, nullptr,
+                          nullptr, page_table, max_pages, live_tags, expected_tags, abort_mask, B,
+                          Hkv, D, page_size, num_pages, stream);
+}
+
+extern "C" int fpk_quantize_e4m3(const float* x, const float* scale, uint8_t* out, int64_t n,
+                                 void* stream) {
+  if (n < 0) return FPK_EINVAL;
+  if (n == 0) return FPK_OK;
+  if (!x || !scale || !out) return FPK_EINVAL;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int64_t want = ((n >> 1) + 255) / 256 + 1;
+  const int64_t cap = static_cast<int64_t>(fpk::device_sm_count(dev) > 0 ? fpk::device_sm_count(dev) : 132) * 32;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  fpk::quantize_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, scale, out, n);
+  return fpk::checked_launch_status();
+}

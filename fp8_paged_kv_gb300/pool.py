@@ -1,0 +1,154 @@
+"""Device-resident decode pool: torch allocates, libfp8kv computes.
+
+A DecodePool holds one layer's paged KV cache (e4m3 or bf16), the page table,
+the live and expected page tags, the per-tensor scales and the output and
+workspace buffers of a decode batch, and runs the decode step in the order
+the pages describe: write the new token's K/V into its page, check every
+request's (page, tag) mapping in a separate batched operation, then attend
+over the pages of the requests that passed.  All arithmetic runs in the
+library's kernels (see fp8_paged_kv_gb300.__init__); this module only moves
+arrays between numpy and the device.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (fpk_decode_workspace_bytes, fpk_kv_append_bf16, fpk_kv_append_fp8,
+               fpk_kv_prefill_bf16, fpk_kv_prefill_fp8, fpk_page_tags_bump,
+               fpk_page_tags_validate, fpk_paged_decode_attn_bf16, fpk_paged_decode_attn_fp8)
+
+NAN_E4M3 = 0x7F          # e4m3 NaN code: fills slots no token was written to
+NAN_BF16 = 0x7FC0
+
+
+def to_device(a: np.ndarray, device) -> torch.Tensor:
+    """numpy -> CUDA tensor; uint32 tags travel as int32, bf16 bits as bfloat16."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint32:
+        a = a.view(np.int32)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+class DecodePool:
+    def __init__(self, wl, fp8: bool = True, device="cuda", num_splits: int | None = None):
+        self.wl = wl
+        self.fp8 = fp8
+        self.device = torch.device(device)
+        dev = self.device
+        n = wl.num_pages * wl.Hkv * wl.page_size * wl.D
+        if fp8:
+            self.k_pool = torch.full((n,), NAN_E4M3, dtype=torch.uint8, device=dev)
+            self.v_pool = torch.full((n,), NAN_E4M3, dtype=torch.uint8, device=dev)
+        else:
+            self.k_pool = torch.full((n,), NAN_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+            self.v_pool = torch.full((n,), NAN_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        self.page_table = to_device(wl.page_table, dev)
+        self.live_tags = to_device(wl.live_tags, dev)
+        self.expected_tags = to_device(wl.expected_tags, dev)
+        self.k_scale = torch.tensor([float(wl.k_scale)], dtype=torch.float32, device=dev)
+        self.v_scale = torch.tensor([float(wl.v_scale)], dtype=torch.float32, device=dev)
+        self.seq_lens = to_device(wl.prompt_lens.astype(np.int32), dev)
+        self.abort_mask = torch.zeros(wl.B, dtype=torch.uint8, device=dev)
+        self.abort_count = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.q = to_device(wl.q, dev)
+        self.out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((wl.B, wl.Hq), dtype=torch.float32, device=dev)
+        self.num_splits = wl.num_splits if num_splits is None else num_splits
+        ws = fpk_decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, self.num_splits)
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.k_new = None
+        self.v_new = None
+
+    @property
+    def kw(self):
+        w = self.wl
+        return dict(Hkv=w.Hkv, D=w.D, page_size=w.page_size, num_pages=w.num_pages)
+
+    # ---------------------------------------------------------------- writes
+    def prefill(self, chunk_tokens: int = 1 << 22):
+        """Bulk-write every request's prompt (positions 0..prompt_len-1)."""
+        wl = self.wl
+        B = wl.B
+        cu = wl.cu_prompt.astype(np.int64)
+        r0 = 0
+        while r0 < B:
+            r1 = r0 + 1
+            while r1 < B and cu[r1 + 1] - cu[r0] <= chunk_tokens:
+                r1 += 1
+            # requests [r0, r1) in one call: a page table with only their rows
+            k = to_device(wl.k_prompt[cu[r0]:cu[r1]], self.device)
+            v = to_device(wl.v_prompt[cu[r0]:cu[r1]], self.device)
+            cu_sub = to_device((cu[r0:r1 + 1] - cu[r0]).astype(np.int32), self.device)
+            pt = self.page_table[r0:r1]
+            ex = self.expected_tags[r0:r1]
+            if self.fp8:
+                fpk_kv_prefill_fp8(k, v, cu_sub, self.k_pool, self.v_pool, self.k_scale, self.v_scale,
+                                   pt, self.live_tags, ex, None, **self.kw)
+            else:
+                fpk_kv_prefill_bf16(k, v, cu_sub, self.k_pool, self.v_pool, pt, self.live_tags, ex,
+                                    None, **self.kw)
+            del k, v
+            r0 = r1
+        torch.cuda.synchronize(self.device)
+
+    def set_step(self, step: int):
+        """Upload decode step `step`'s new K/V rows, query and context lengths."""
+        kn, vn = self.wl.step_tokens(step)
+        self.k_new = to_device(kn, self.device)
+        self.v_new = to_device(vn, self.device)
+        self.q = to_device(self.wl.step_query(step), self.device)
+        self.seq_lens = to_device(self.wl.seq_lens_after(step), self.device)
+
+    def append(self, stream=None, guard: bool = True):
+        tags = (self.live_tags, self.expected_tags, self.abort_mask) if guard else (None, None, None)
+        if self.fp8:
+            fpk_kv_append_fp8(self.k_new, self.v_new, self.k_pool, self.v_pool, self.k_scale,
+                              self.v_scale, self.page_table, self.seq_lens, *tags, stream=stream,
+                              **self.kw)
+        else:
+            fpk_kv_append_bf16(self.k_new, self.v_new, self.k_pool, self.v_pool, self.page_table,
+                               self.seq_lens, *tags, stream=stream, **self.kw)
+
+    # ----------------------------------------------------------------- tags
+    def bump(self, pages: torch.Tensor, stream=None):
+        fpk_page_tags_bump(self.live_tags, pages, num_pages=self.wl.num_pages, stream=stream)
+
+    def validate(self, stream=None):
+        fpk_page_tags_validate(self.page_table, self.expected_tags, self.seq_lens, self.live_tags,
+                               self.abort_mask, self.abort_count, num_pages=self.wl.num_pages,
+                               page_size=self.wl.page_size, stream=stream)
+
+    # ------------------------------------------------------------ attention
+    def attend(self, use_mask: bool = True, stream=None, num_splits: int | None = None):
+        wl = self.wl
+        ns = self.num_splits if num_splits is None else num_splits
+        mask = self.abort_mask if use_mask else None
+        kw = dict(Hkv=wl.Hkv, page_size=wl.page_size, num_pages=wl.num_pages,
+                  sm_scale=wl.sm_scale, num_splits=ns, stream=stream)
+        if self.fp8:
+            fpk_paged_decode_attn_fp8(self.q, self.k_pool, self.v_pool, self.k_scale, self.v_scale,
+                                      self.page_table, self.seq_lens, mask, self.out, self.lse,
+                                      self.workspace, **kw)
+        else:
+            fpk_paged_decode_attn_bf16(self.q, self.k_pool, self.v_pool, self.page_table,
+                                       self.seq_lens, mask, self.out, self.lse, self.workspace, **kw)
+
+    def step(self, validate: bool = True, stream=None):
+        """One decode step: append, (validate), attend."""
+        self.append(stream=stream)
+        if validate:
+            self.validate(stream=stream)
+            self.attend(use_mask=True, stream=stream)
+        else:
+            self.attend(use_mask=False, stream=stream)
+
+    # ------------------------------------------------------------- readback
+    def pool_bytes(self):
+        """Host copies of the pools as raw uint8 / uint16 numpy arrays."""
+        if self.fp8:
+            return self.k_pool.cpu().numpy(), self.v_pool.cpu().numpy()
+        return (self.k_pool.view(torch.int16).cpu().numpy().view(np.uint16),
+                self.v_pool.view(torch.int16).cpu().numpy().view(np.uint16))

@@ -1,0 +1,254 @@
+/*
+ * fp8kv.h -- C ABI of libfp8kv, the GB300 (sm_103a) decode-pool hot path over
+ * a paged FP8 e4m3 KV cache with page-tag integrity checks.
+ *
+ * What it implements is described by the Cloudflare Workers AI write-up on
+ * serving Kimi K2.6 and GLM 5.2 (reported by "Il serving di modelli piu
+ * piccoli di Cloudflare riduce la memoria, ma la sicurezza diventa la prova
+ * decisiva", remio.ai, and its Portuguese and Korean editions; and by the
+ * iitog.ru and manulx.blog summaries):
+ *   - the KV cache of the decode pool is stored as FP8 e4m3 in place of BF16,
+ *     halving its bytes (section "Cosa ha cambiato Cloudflare per Kimi e GLM");
+ *   - the attention kernel converts the FP8 values as it reads them (section
+ *     "Perche le cache piu piccole di Cloudflare battono la velocita pura");
+ *   - every physical page carries a tag that changes on each reallocation, the
+ *     server records the (page, tag) pairs each request expects, and a separate
+ *     batched check compares them before supported decode operations read the
+ *     pages; a mismatch aborts that request (sections "Cosa ha cambiato..." and
+ *     "La sicurezza della cache KV condivisa diventa una questione di
+ *     produzione"); with the check off, a no-op tracker costs nothing.
+ * The pages give no kernel design and no layouts: every layout and schedule
+ * below is this library's own.
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions for every entry point
+ * ---------------------------------------------------------------------------
+ * Pointers: every array argument is a DEVICE pointer unless stated otherwise.
+ * The caller owns all memory; the library allocates nothing, keeps no
+ * per-call state and launches only on the given stream (`stream` is a
+ * cudaStream_t passed as void*; NULL means the legacy default stream).  All
+ * calls are asynchronous with respect to the host; synchronise the stream
+ * before reading results.
+ *
+ * Shapes: B requests, Hq query heads, Hkv kv heads (G = Hq/Hkv query heads
+ * share one kv head: query head h reads kv head h / G), head dimension D,
+ * page_size tokens per physical page, num_pages pages in the pool, max_pages
+ * columns in each request's page table.
+ *
+ * Supported sizes: D == 128; page_size a multiple of 16 in [16, 256];
+ * 1 <= G <= 8; B, Hkv >= 1.  Others return FPK_EUNSUPPORTED.
+ *
+ * Pool layout (bytes per element: 1 for the e4m3 pool, 2 for the bf16 pool):
+ *   K pool  [num_pages][Hkv][page_size][D]           token-major rows
+ *   V pool  [num_pages][Hkv][page_size/16][D][16]     16-token column blocks,
+ *                                                     dim-major inside a block
+ *   Token t of a request lives in page page_table[r][t / page_size] at slot
+ *   t % page_size.  Pool base pointers must be 16-byte aligned.
+ * Page table:     int32  [B][max_pages]   (row-major; entries past a request's
+ *                                          ceil(L/page_size) pages are ignored)
+ * Expected tags:  uint32 [B][max_pages]   (same shape as the page table)
+ * Live tags:      uint32 [num_pages]
+ * seq_lens:       int32  [B]              context length L_r of each request
+ * Scales:         float  [1] each         per-tensor dequantisation scale:
+ *                 value = decode_e4m3(code) * scale; positive and finite.
+ *
+ * E4M3 is the OCP OFP8 E4M3 format (bias 7, no infinities, NaN = S.1111.111,
+ * largest finite 448).  Quantisation computes float(x)/scale with one IEEE
+ * fp32 division and rounds to nearest-even with saturation to +-448; NaN
+ * encodes as 0x7F.
+ *
+ * Errors: the return value is synchronous.  FPK_OK on success;
+ * FPK_EINVAL for a NULL required pointer, a negative size or Hq % Hkv != 0;
+ * FPK_EUNSUPPORTED for sizes outside the supported set; FPK_ENOSPC when a
+ * workspace is too small; FPK_ECUDA when a launch fails (the CUDA error is
+ * left pending for the caller to read).  Data faults -- a stale tag, a page id
+ * outside [0, num_pages), a context longer than the page table -- are never API
+ * errors: they fail closed per request (no page of that request is read or
+ * written, its attention output is 0 and its lse is -inf) and are reported in
+ * abort_mask / abort_count where those are given.
+ */
+#ifndef FP8KV_H_
+#define FP8KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FPK_OK 0
+#define FPK_EINVAL 1
+#define FPK_EUNSUPPORTED 2
+#define FPK_ENOSPC 3
+#define FPK_ECUDA 4
+
+/* Library ABI version (major * 100 + minor). */
+int fpk_version(void);
+
+/* Human-readable text for a status code (static storage; never NULL). */
+const char* fpk_status_str(int status);
+
+/*
+ * Quantise-on-append for one decode step (FP8 cache).
+ * Source: "Cosa ha cambiato Cloudflare per Kimi e GLM" (the cache is held as
+ * e4m3) and the iitog.ru summary's third technique (requests write the pages
+ * of the shared cache).
+ *
+ * For every request r with L = seq_lens[r] >= 1 (seq_lens already counts the
+ * new token) and every kv head h and dim d, writes
+ *   k_pool[page][h][pos % page_size][d] = e4m3(float(k_new[r][h][d]) / *k_scale)
+ * and the V value into its column block, pos = L - 1,
+ * page = page_table[r][pos / page_size].
+ * Guard (fail closed): when pos / page_size >= max_pages, the page id is
+ * outside [0, num_pages), or live_tags and expected_tags are both given and
+ * live_tags[page] != expected_tags[r][pos / page_size], nothing of request r
+ * is written and abort_mask[r] is set to 1 (if abort_mask is non-NULL; other
+ * entries are left as they are).
+ *   k_new, v_new : bf16 [B][Hkv][D] (device)
+ *   live_tags, expected_tags, abort_mask : nullable (NULL = no tag guard)
+ */
+int fpk_kv_append_fp8(const void* k_new, const void* v_new, uint8_t* k_pool, uint8_t* v_pool,
+                      const float* k_scale, const float* v_scale,
+                      const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                      const uint32_t* live_tags, const uint32_t* expected_tags,
+                      uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
+                      int32_t page_size, int32_t num_pages, void* stream);
+
+/* Same as fpk_kv_append_fp8 for the BF16 comparison cache: the bf16 bit
+ * patterns are copied unchanged (pools hold uint16 elements).  The pages keep
+ * BF16 caches where compute dominates ("Cosa ha cambiato...", last paragraphs). */
+int fpk_kv_append_bf16(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                       const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                       const uint32_t* live_tags, const uint32_t* expected_tags,
+                       uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
+                       int32_t page_size, int32_t num_pages, void* stream);
+
+/*
+ * Bulk write of whole prompts into the pages (the cache a decode pool receives
+ * from prefill).  Rows cu_seqlens[r] .. cu_seqlens[r+1]-1 of k, v (bf16
+ * [n_tokens][Hkv][D]) are request r's tokens at positions 0, 1, ...; each token
+ * is written exactly as fpk_kv_append_fp8 writes one, with the same guard.
+ *   cu_seqlens : int32 [B+1] (device), cu_seqlens[0] == 0, non-decreasing,
+ *                cu_seqlens[B] == n_tokens.
+ */
+int fpk_kv_prefill_fp8(const void* k, const void* v, const int32_t* cu_seqlens, int32_t n_tokens,
+                       uint8_t* k_pool, uint8_t* v_pool, const float* k_scale, const float* v_scale,
+                       const int32_t* page_table, int32_t max_pages,
+                       const uint32_t* live_tags, const uint32_t* expected_tags,
+                       uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
+                       int32_t page_size, int32_t num_pages, void* stream);
+
+/* BF16-cache variant of fpk_kv_prefill_fp8 (bit copy). */
+int fpk_kv_prefill_bf16(const void* k, const void* v, const int32_t* cu_seqlens, int32_t n_tokens,
+                        void* k_pool, void* v_pool, const int32_t* page_table, int32_t max_pages,
+                        const uint32_t* live_tags, const uint32_t* expected_tags,
+                        uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
+                        int32_t page_size, int32_t num_pages, void* stream);
+
+/*
+ * Element-wise quantiser: out[i] = e4m3(x[i] / *scale) for i < n, with the
+ * same division and rounding as the append.  x: float [n], out: uint8 [n].
+ */
+int fpk_quantize_e4m3(const float* x, const float* scale, uint8_t* out, int64_t n, void* stream);
+
+/*
+ * Page reallocation: live_tags[pages[i]] += 1 (mod 2^32) for i < n.
+ * Source: "Cosa ha cambiato..." -- a page's tag changes every time the page is
+ * reallocated; "La sicurezza della cache KV condivisa..." -- the tags behave
+ * like generation counters.  Ids outside [0, num_pages) are ignored; an id
+ * listed k times advances by k.  n == 0 launches nothing.
+ *   pages : int32 [n] (device)
+ */
+int fpk_page_tags_bump(uint32_t* live_tags, const int32_t* pages, int32_t n, int32_t num_pages,
+                       void* stream);
+
+/*
+ * Batched page-tag validation, a separate pure gather-compare that runs before
+ * attention (never fused into it: "La sicurezza della cache KV condivisa..."
+ * says the check was kept out of the attention kernel because of races
+ * between GPU thread groups).
+ * For every request r, with P = ceil(seq_lens[r] / page_size) (0 if L <= 0):
+ *   abort_mask[r] = 1 iff P > max_pages, or some i < P has page_table[r][i]
+ *   outside [0, num_pages) or live_tags[page_table[r][i]] != expected_tags[r][i];
+ *   otherwise abort_mask[r] = 0 (the mask is overwritten).
+ *   abort_count (nullable, int32 [1]) receives the number of aborted requests
+ *   (the mismatch-rate signal the pages ask operators to watch).
+ */
+int fpk_page_tags_validate(const int32_t* page_table, const uint32_t* expected_tags,
+                           const int32_t* seq_lens, int32_t max_pages,
+                           const uint32_t* live_tags, int32_t num_pages, int32_t B,
+                           int32_t page_size, uint8_t* abort_mask, int32_t* abort_count,
+                           void* stream);
+
+/*
+ * Workspace (device bytes) that fpk_paged_decode_attn_* needs for this batch
+ * shape and split count.  num_splits == 0 means the automatic count the
+ * attention call would choose on the CURRENT device.
+ */
+size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t num_splits);
+
+/*
+ * Split-KV decode attention over the FP8 e4m3 cache, dequantising on read,
+ * with the cross-split log-sum-exp combine.
+ * Sources: "Perche le cache piu piccole..." (the kernel converts FP8 on read),
+ * "La sicurezza della cache KV condivisa..." (paged attention over physical
+ * pages; aborted requests read nothing).
+ *
+ * For request r, query head h, kv head hk = h / G, tokens j < L = seq_lens[r]:
+ *   s_j   = sm_scale * sum_d q[r][h][d] * decode(K code) * *k_scale
+ *   out[r][h][:] = sum_j exp(s_j - m) * decode(V code) * *v_scale / sum_j exp(s_j - m)
+ *   lse[r][h]    = m + ln(sum_j exp(s_j - m)),   m = max_j s_j
+ * A request with L <= 0, abort_mask[r] != 0, L > max_pages * page_size, or a
+ * page id outside [0, num_pages) among its first ceil(L/page_size) entries
+ * gets out = 0 and lse = -inf, and (except for the last case, found while
+ * streaming) none of its pages is read.
+ *   q         : bf16 [B][Hq][D]
+ *   abort_mask: uint8 [B] from fpk_page_tags_validate, or NULL (no-op tracker:
+ *               no tag check)
+ *   out       : float [B][Hq][D];  lse: float [B][Hq], nullable
+ *   workspace : >= fpk_decode_workspace_bytes(...) bytes, 256-byte aligned,
+ *               owned by the caller.  Zero it ONCE after allocating: it holds
+ *               per-segment arrival counters that every call leaves at zero
+ *               again, split partials, and in its first 4 bytes a status word
+ *               the kernel sets to nonzero (and never clears) if a bounded
+ *               internal wait gave up; read it with fpk_decode_status and
+ *               re-zero the whole workspace after a nonzero status.  Calls
+ *               that share a workspace must not overlap on the GPU.
+ *   num_splits: number of split-KV work units the batch's KV tiles are
+ *               divided into (balanced by tile count across all requests and
+ *               kv heads); 0 = automatic (fills the GPU once).  With equal
+ *               context lengths, num_splits = S * B * Hkv gives exactly S
+ *               splits per (request, kv head).
+ *   sm_scale  : softmax scale (1/sqrt(D) for standard attention).
+ */
+int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* page_table, int32_t max_pages,
+                              const int32_t* seq_lens, const uint8_t* abort_mask,
+                              float* out, float* lse, void* workspace, size_t workspace_bytes,
+                              int32_t num_splits, float sm_scale, int32_t B, int32_t Hq,
+                              int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                              void* stream);
+
+/* BF16-cache variant of fpk_paged_decode_attn_fp8: same semantics with
+ * k_pool / v_pool holding bf16 values (no scales). */
+int fpk_paged_decode_attn_bf16(const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* page_table, int32_t max_pages,
+                               const int32_t* seq_lens, const uint8_t* abort_mask,
+                               float* out, float* lse, void* workspace, size_t workspace_bytes,
+                               int32_t num_splits, float sm_scale, int32_t B, int32_t Hq,
+                               int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                               void* stream);
+
+/*
+ * Copies the workspace status word to *status (HOST pointer) and synchronises
+ * the stream.  0 means no bounded wait inside the attention kernels gave up.
+ */
+int fpk_decode_status(const void* workspace, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8KV_H_ */

@@ -1,0 +1,80 @@
+"""The C-ABI library builds for sm_103a, loads and exports every entry point
+that include/fp8kv.h declares, and the Python binding mirrors them (no compute
+call is made here: this runs on hosts without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8kv.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fpk_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_paged_kv_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_path():
+    syms = declared_symbols()
+    for name in ("fpk_kv_append_fp8", "fpk_kv_append_bf16", "fpk_page_tags_bump",
+                 "fpk_page_tags_validate", "fpk_paged_decode_attn_fp8",
+                 "fpk_paged_decode_attn_bf16", "fpk_decode_workspace_bytes", "fpk_status_str"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_binding_mirrors_the_header():
+    import fp8_paged_kv_gb300 as fpk
+    assert set(fpk.SIGNATURES) == set(declared_symbols())
+    for name in declared_symbols():
+        if name not in ("fpk_version", "fpk_status_str"):
+            assert callable(getattr(fpk, name)), name
+
+
+def test_host_only_entry_points(lib):
+    lib.fpk_version.restype = ctypes.c_int
+    lib.fpk_status_str.restype = ctypes.c_char_p
+    assert lib.fpk_version() >= 100
+    for s in range(5):
+        assert lib.fpk_status_str(s)
+    assert b"unknown" in lib.fpk_status_str(99)
+
+
+def test_argument_errors_are_synchronous_without_a_device(lib):
+    """Invalid arguments are rejected before anything touches a device."""
+    f = lib.fpk_page_tags_bump
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+    assert f(None, None, -1, 4, None) == 1          # FPK_EINVAL
+    assert f(None, None, 0, 4, None) == 0           # nothing to do
+    g = lib.fpk_decode_workspace_bytes
+    g.restype = ctypes.c_size_t
+    g.argtypes = [ctypes.c_int32] * 5
+    assert g(4, 64, 7, 128, 16) == 0                 # Hq % Hkv != 0
+    assert g(4, 64, 8, 64, 16) == 0                  # unsupported D
+    assert g(4, 64, 8, 128, 16) > 0                  # fixed split count needs no device
+
+
+def test_no_oracle_in_the_product():
+    """The product package never imports or links the oracle."""
+    pkg = os.path.join(ROOT, "fp8_paged_kv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "fp8kv_oracle" not in text, f

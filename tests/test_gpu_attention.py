@@ -1,0 +1,218 @@
+"""GPU parity of split-KV paged decode attention (FP8 and BF16 caches).
+
+Every case runs the CUDA path through the C ABI and the fp64 oracle on the
+same seeded inputs; outputs must satisfy |gpu - ref| <= 2e-3 + 1e-2 |ref|
+(lse likewise), and dead requests (aborted, empty, over-long, bad page id)
+must give exactly 0 and lse = -inf.  Small cases span several tiles, ragged
+last tiles, every supported group size, several page sizes and split counts;
+the full-size workloads run in the benchmark's launch configuration and are
+checked on sampled requests.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_paged_kv_gb300 import fpk_decode_workspace_bytes
+from fp8_paged_kv_gb300.pool import DecodePool, to_device
+from tests.gpu_helpers import assert_attention_close, oracle_attention, oracle_pools
+from workloads import b32_8k, b64_var, custom, long128k, rng_for, tiny
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+_cache = {}
+
+
+def _wl(fn, **kw):
+    key = (fn.__name__, tuple(sorted(kw.items())))
+    if key not in _cache:
+        _cache.clear()          # keep at most one full-size workload in host memory
+        _cache[key] = fn(**kw)
+    return _cache[key]
+
+
+def _run_case(wl, fp8, num_splits, abort=None, use_mask=True, pt_override=None):
+    pool = DecodePool(wl, fp8=fp8, device=DEV, num_splits=num_splits)
+    pool.prefill()
+    lens = wl.prompt_lens.astype(np.int32)
+    if pt_override is not None:
+        pool.page_table = to_device(pt_override, DEV)
+    if abort is not None:
+        pool.abort_mask = to_device(abort.astype(np.uint8), DEV)
+    pool.attend(use_mask=use_mask)
+    torch.cuda.synchronize()
+    assert pool.workspace[:4].view(torch.int32).item() == 0, "bounded wait gave up"
+    kp, vp = oracle_pools(wl, fp8)
+    ref_out, ref_lse = oracle_attention(wl, kp, vp, fp8, wl.q, lens,
+                                        abort=abort if use_mask else None, page_table=pt_override)
+    return pool.out.cpu().numpy(), pool.lse.cpu().numpy(), ref_out, ref_lse
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("ps", [16, 64])
+def test_small_ragged(fp8, G, ps):
+    Hkv = 2
+    lens = [0, 1, 15, 16, 17, 100, 3 * ps + 7, 257]
+    wl = custom(61 + G + ps, B=len(lens), Hq=G * Hkv, Hkv=Hkv, ps=ps, prompt_lens=lens, steps=0,
+                sigma=1.5, outlier_frac=0.02)
+    out, lse, ro, rl = _run_case(wl, fp8, num_splits=0)
+    assert_attention_close(out, lse, ro, rl, f"fp8={fp8} G={G} ps={ps}")
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("num_splits", [1, 2, 5, 37, 300, 4096])
+def test_split_counts(fp8, num_splits):
+    lens = [700, 33, 0, 1025, 64, 5]
+    wl = custom(70 + num_splits, B=len(lens), Hq=16, Hkv=2, ps=16, prompt_lens=lens, steps=0)
+    out, lse, ro, rl = _run_case(wl, fp8, num_splits=num_splits)
+    assert_attention_close(out, lse, ro, rl, f"splits={num_splits}")
+
+
+def test_split_invariance():
+    lens = [3000, 1, 900]
+    wl = custom(80, B=3, Hq=32, Hkv=4, ps=32, prompt_lens=lens, steps=0)
+    pool = DecodePool(wl, fp8=True, device=DEV)
+    pool.prefill()
+    # one workspace large enough for every split count used below
+    need = max(fpk_decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, ns) for ns in (0, 1000))
+    pool.workspace = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    outs = []
+    for ns in (0, 1, 7, 64, 1000):
+        pool.attend(num_splits=ns)
+        outs.append(pool.out.cpu().numpy().copy())
+    # P is rounded to f16 (relative 2^-11) against a running max that depends on
+    # where splits start, so results agree to about 2^-10 * max|V| across splits
+    bound = 2.0 ** -10 * 448.0 * float(wl.v_scale)     # 448 * v_scale = max |V-hat|
+    for o in outs[1:]:
+        assert np.max(np.abs(o - outs[0])) < bound
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+def test_abort_mask_and_noop_tracker(fp8):
+    lens = [40, 90, 17, 300]
+    wl = custom(81, B=4, Hq=16, Hkv=2, ps=16, prompt_lens=lens, steps=0)
+    abort = np.array([0, 1, 0, 1], np.uint8)
+    out, lse, ro, rl = _run_case(wl, fp8, 0, abort=abort, use_mask=True)
+    assert_attention_close(out, lse, ro, rl, "masked")
+    assert np.isneginf(lse[[1, 3]]).all() and not out[[1, 3]].any()
+    # the no-op tracker (no mask) ignores tags and attends everything
+    out, lse, ro, rl = _run_case(wl, fp8, 0, abort=abort, use_mask=False)
+    assert_attention_close(out, lse, ro, rl, "no-op tracker")
+    assert np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("num_splits", [0, 3, 64])
+def test_bad_page_id_fails_closed_without_tracker(num_splits):
+    lens = [200, 200, 200]
+    wl = custom(82, B=3, Hq=8, Hkv=2, ps=16, prompt_lens=lens, steps=0)
+    pt = wl.page_table.copy()
+    pt[1, 5] = wl.num_pages + 1000        # would read past the pool
+    pt[2, 0] = -2
+    out, lse, ro, rl = _run_case(wl, True, num_splits, use_mask=False, pt_override=pt)
+    assert_attention_close(out, lse, ro, rl, "bad page")
+    assert np.isneginf(lse[1:]).all() and not out[1:].any()
+
+
+def test_overlong_context_is_dead():
+    wl = custom(83, B=2, Hq=8, Hkv=2, ps=16, prompt_lens=[40, 40], steps=0)
+    pool = DecodePool(wl, fp8=True, device=DEV)
+    pool.prefill()
+    lens = np.array([40, wl.max_pages * 16 + 1], np.int32)
+    pool.seq_lens = to_device(lens, DEV)
+    pool.attend(use_mask=False)
+    out, lse = pool.out.cpu().numpy(), pool.lse.cpu().numpy()
+    assert np.isneginf(lse[1]).all() and not out[1].any() and np.isfinite(lse[0]).all()
+
+
+def test_tiny_full_step():
+    """The tiny workload end to end: prefill, append, validate, attend."""
+    wl = tiny()
+    pool = DecodePool(wl, fp8=True, device=DEV)
+    pool.prefill()
+    pool.set_step(0)
+    pool.step(validate=True)
+    torch.cuda.synchronize()
+    kp, vp = oracle_pools(wl, True)
+    kn, vn = wl.step_tokens(0)
+    lens = wl.seq_lens_after(0)
+    mask0 = np.zeros(2, np.uint8)
+    oracle.kv_append(kn, vn, kp, vp, wl.k_scale, wl.v_scale, wl.page_table, lens, wl.live_tags,
+                     wl.expected_tags, mask0, fp8=True, Hkv=wl.Hkv, D=wl.D, page_size=16,
+                     num_pages=wl.num_pages)
+    gk, gv = pool.pool_bytes()
+    assert np.array_equal(gk, kp) and np.array_equal(gv, vp)
+    mask, n = oracle.page_tags_validate(wl.page_table, wl.expected_tags, lens, wl.live_tags,
+                                        wl.num_pages, 16)
+    assert list(mask) == [0, 1] and np.array_equal(pool.abort_mask.cpu().numpy(), mask)
+    ro, rl = oracle_attention(wl, kp, vp, True, wl.q, lens, abort=mask)
+    assert_attention_close(pool.out.cpu().numpy(), pool.lse.cpu().numpy(), ro, rl, "tiny")
+
+
+def _sampled_full_size(wl, fp8, rows, steps=1, num_splits=None):
+    """Run `steps` decode steps (append, validate, attend) at full size and check
+    the sampled requests' cache bytes and attention against the oracle."""
+    pool = DecodePool(wl, fp8=fp8, device=DEV, num_splits=num_splits)
+    pool.prefill()
+    for s in range(steps):
+        pool.set_step(s)
+        pool.step(validate=True)
+        torch.cuda.synchronize()
+        lens = wl.seq_lens_after(s)
+        mask, n = oracle.page_tags_validate(wl.page_table, wl.expected_tags, lens, wl.live_tags,
+                                            wl.num_pages, wl.page_size)
+        assert np.array_equal(pool.abort_mask.cpu().numpy(), mask), f"abort set, step {s}"
+        assert int(pool.abort_count.item()) == n
+    assert pool.workspace[:4].view(torch.int32).item() == 0
+    # oracle cache of the sampled requests only
+    dt = np.uint8 if fp8 else np.uint16
+    npool = wl.num_pages * wl.Hkv * wl.page_size * wl.D
+    kp = np.full(npool, 0x7F if fp8 else 0x7FC0, dt)
+    vp = np.full(npool, 0x7F if fp8 else 0x7FC0, dt)
+    for r in rows:
+        a, b = int(wl.cu_prompt[r]), int(wl.cu_prompt[r + 1])
+        cu = np.array([0, b - a], np.int32)
+        oracle.kv_prefill(wl.k_prompt[a:b], wl.v_prompt[a:b], cu, kp, vp, wl.k_scale, wl.v_scale,
+                          wl.page_table[r:r + 1], wl.live_tags, wl.expected_tags[r:r + 1], None,
+                          fp8=fp8, Hkv=wl.Hkv, D=wl.D, page_size=wl.page_size,
+                          num_pages=wl.num_pages)
+    for s in range(steps):
+        kn, vn = wl.step_tokens(s)
+        lens = wl.seq_lens_after(s)
+        for r in rows:
+            oracle.kv_append(kn[r:r + 1], vn[r:r + 1], kp, vp, wl.k_scale, wl.v_scale,
+                             wl.page_table[r:r + 1], lens[r:r + 1], wl.live_tags,
+                             wl.expected_tags[r:r + 1], None, fp8=fp8, Hkv=wl.Hkv, D=wl.D,
+                             page_size=wl.page_size, num_pages=wl.num_pages)
+    gk, gv = pool.pool_bytes()
+    for r in rows:
+        P = -(-int(wl.seq_lens_after(steps - 1)[r]) // wl.page_size)
+        blk = wl.Hkv * wl.page_size * wl.D
+        for page in wl.page_table[r, :P]:
+            sl = slice(int(page) * blk, (int(page) + 1) * blk)
+            assert np.array_equal(gk[sl], kp[sl]) and np.array_equal(gv[sl], vp[sl]), (r, page)
+    lens = wl.seq_lens_after(steps - 1)
+    q = wl.step_query(steps - 1)
+    ro, rl = oracle_attention(wl, kp, vp, fp8, q, lens, rows=rows)
+    out = pool.out.cpu().numpy()[rows]
+    lse = pool.lse.cpu().numpy()[rows]
+    return assert_attention_close(out, lse, ro, rl, f"{wl.name} fp8={fp8}")
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+def test_b32_8k_full_size_sampled(fp8):
+    wl = _wl(b32_8k)
+    _sampled_full_size(wl, fp8, rows=[0, 31], steps=1)
+
+
+def test_b64_var_full_size_sampled():
+    wl = _wl(b64_var, steps=3)
+    g = rng_for(3, "sample")
+    rows = sorted(set([int(np.argmax(wl.prompt_lens)), int(np.argmin(wl.prompt_lens)),
+                       int(g.integers(0, 64))]))
+    _sampled_full_size(wl, True, rows=rows, steps=3)
+
+
+def test_long128k_full_size_sampled_64_splits():
+    wl = _wl(long128k)
+    _sampled_full_size(wl, True, rows=[2], steps=1, num_splits=64 * 4 * 8)
