@@ -51,6 +51,9 @@ SIGNATURES = {
                                                  _P]),
     "fpk_paged_decode_attn_bf16": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ,
                                                   _I32, _F, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
+    "fpk_paged_decode_attn_fp8_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _P, _P,
+                                                         _P, _I32, _F, _I32, _I32, _I32, _I32, _I32,
+                                                         _I32, _P]),
     "fpk_decode_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
 }
 
@@ -228,6 +231,23 @@ def fpk_paged_decode_attn_bf16(q, k_pool, v_pool, page_table, seq_lens, abort_ma
         _ptr(lse, _F32, "lse", True), _ptr(workspace, _U8, "workspace"),
         workspace.numel(), num_splits, sm_scale, B, Hq, Hkv, D, page_size, num_pages,
         _stream(stream)), "fpk_paged_decode_attn_bf16")
+
+
+def fpk_paged_decode_attn_fp8_noalloc(q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens,
+                                      abort_mask, out, lse, *, Hkv, page_size, num_pages, sm_scale,
+                                      num_splits=0, stream=None):
+    """FP8 decode attention without a caller workspace, for callers that cannot
+    allocate device memory; the scratch is a fixed array inside the library
+    (batches needing more than 16 MiB of it are rejected).  Calls that overlap
+    on the GPU share that scratch and race."""
+    B, Hq, D = q.shape
+    _check(load_library().fpk_paged_decode_attn_fp8_noalloc(
+        _ptr(q, _BF16_LIKE, "q"), _ptr(k_pool, _U8, "k_pool"), _ptr(v_pool, _U8, "v_pool"),
+        _ptr(k_scale, _F32, "k_scale"), _ptr(v_scale, _F32, "v_scale"),
+        _ptr(page_table, _I32T, "page_table"), page_table.shape[1], _ptr(seq_lens, _I32T, "seq_lens"),
+        _ptr(abort_mask, _U8, "abort_mask", True), _ptr(out, _F32, "out"),
+        _ptr(lse, _F32, "lse", True), num_splits, sm_scale, B, Hq, Hkv, D, page_size, num_pages,
+        _stream(stream)), "fpk_paged_decode_attn_fp8_noalloc")
 
 
 def fpk_decode_status(workspace, stream=None) -> int:

@@ -809,3 +809,77 @@ extern "C" int fpk_decode_status(const void* workspace, int32_t* status, void* s
   if (cudaStreamSynchronize(s) != cudaSuccess) return FPK_ECUDA;
   return FPK_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the FP8 attention entry point.
+//
+// Some callers cannot allocate device memory for a workspace: operator hosts
+// and plugin interfaces that hand an operator only its inputs and outputs,
+// processes held to a fixed device-memory budget, and latency-critical loops
+// that cannot afford cudaMalloc's implicit device synchronisation.  For them
+// the scratch lives in the file-scope array below, a fixed 16 MiB that every
+// GPU loading this library keeps until the process exits.  In host code the
+// array's name is only a host-side stand-in, so its device address is looked
+// up once per device (with that device current) and passed to the kernel.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace fpk {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// Set-up, once per device: the scratch array's device address on `dev`
+// (which must be the current device).
+int noalloc_scratch_address(int dev, void** addr) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FPK_ECUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *addr = g_noalloc_addr[dev];
+  return FPK_OK;
+}
+
+}  // namespace
+}  // namespace fpk
+
+extern "C" int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k_pool,
+                                                 const uint8_t* v_pool, const float* k_scale,
+                                                 const float* v_scale, const int32_t* page_table,
+                                                 int32_t max_pages, const int32_t* seq_lens,
+                                                 const uint8_t* abort_mask, float* out, float* lse,
+                                                 int32_t num_splits, float sm_scale, int32_t B,
+                                                 int32_t Hq, int32_t Hkv, int32_t D,
+                                                 int32_t page_size, int32_t num_pages,
+                                                 void* stream) {
+  int st = fpk::check_attn_shapes(B, Hq, Hkv, D, page_size, num_pages, max_pages, num_splits);
+  if (st != FPK_OK) return st;
+  if (B == 0) return FPK_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fpk::kMaxDevices) return FPK_ECUDA;
+  void* scratch = nullptr;
+  st = fpk::noalloc_scratch_address(dev, &scratch);
+  if (st != FPK_OK) return st;
+  int W = num_splits;
+  if (W == 0) {
+    const int per_sm = fpk::prepare_kernel<true>(dev);
+    if (per_sm <= 0) return FPK_ECUDA;
+    W = fpk::device_sm_count(dev) * per_sm;
+    if (W <= 0) return FPK_ECUDA;
+  }
+  const fpk::WsLayout l = fpk::layout(B, Hkv, Hq / Hkv, W);
+  if (l.total > fpk::kNoAllocScratchBytes) return FPK_ENOSPC;  // batch too large for the fixed scratch
+  // the status word and the arrival counters must start at zero
+  if (cudaMemsetAsync(scratch, 0, l.part_ml, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FPK_ECUDA;
+  return fpk::attn_entry<true>(q, k_pool, v_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
+                               abort_mask, out, lse, scratch, fpk::kNoAllocScratchBytes, W, sm_scale,
+                               B, Hq, Hkv, D, page_size, num_pages, stream);
+}

@@ -242,6 +242,36 @@ int fpk_paged_decode_attn_bf16(const void* q, const void* k_pool, const void* v_
                                void* stream);
 
 /*
+ * Allocation-free variant of fpk_paged_decode_attn_fp8 (same arguments and
+ * results, minus the workspace).  The write-up has no counterpart of this
+ * entry point; it exists for callers that cannot allocate device memory --
+ * operator hosts and plugin interfaces that hand an operator only its inputs
+ * and outputs, processes held to a fixed device-memory budget, and
+ * latency-critical loops that cannot afford cudaMalloc's implicit device
+ * synchronisation.  The caller still passes q, the pools, tables, out and lse.
+ *
+ * Scratch: a fixed 16 MiB array inside the library, which every GPU that
+ * loads the library holds until the process exits.  A batch whose workspace
+ * (fpk_decode_workspace_bytes) would exceed 16 MiB is rejected with
+ * FPK_ENOSPC before anything is launched.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ * Set-up: the first call on a device looks up the array's device address on
+ * that device (the device current at the call); make that first call before
+ * any stream capture.
+ * Sharing: every call on a device uses the same array and clears its status
+ * word and counters first; calls that overlap on the GPU (other streams or
+ * other host threads) race on it and must be serialised by the caller.  The
+ * kernel's status word is not reported by this entry point.
+ */
+int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* page_table, int32_t max_pages,
+                                      const int32_t* seq_lens, const uint8_t* abort_mask,
+                                      float* out, float* lse, int32_t num_splits, float sm_scale,
+                                      int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                      int32_t page_size, int32_t num_pages, void* stream);
+
+/*
  * Copies the workspace status word to *status (HOST pointer) and synchronises
  * the stream.  0 means no bounded wait inside the attention kernels gave up.
  */
