@@ -54,9 +54,10 @@ template <bool kFp8>
 struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kBlockBytes = kTile * kDim * kElem;  // one K (or V) tile
-  static constexpr int kStageBytes = 2 * kBlockBytes;
-  static constexpr int kStages = kFp8 ? 16 : 8;
-  // Within a segment piece consumer warp c takes tiles c, c+4, ...; with
+  // a stage holds two consecutive tiles: [K tile 0][K tile 1][V tile 0][V tile 1]
+  static constexpr int kStageBytes = 4 * kBlockBytes;
+  static constexpr int kStages = kFp8 ? 8 : 4;
+  // Within a segment piece consumer warp c takes stages c, c+4, ...; with
   // kStages a multiple of the warp count, the previous round of a stage was
   // consumed by the same warp, so no warp ever waits on a stage's mbarrier
   // while its previous phase is still pending (the parity test would alias
@@ -64,7 +65,9 @@ struct Cfg {
   static_assert(kStages % kConsumerWarps == 0, "ring stages must be a multiple of the consumer warps");
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kMergeBytes = kConsumerWarps * kGroupMax * kMergeStride * 4;
-  static constexpr int kMlBytes = kConsumerWarps * kGroupMax * 4 * 2 + kConsumerWarps * 4;
+  // (m, l) per warp and head, then one fault flag per warp; rounded to 16 bytes
+  // so that the mbarriers that follow stay 8-byte aligned for any warp count
+  static constexpr int kMlBytes = (kConsumerWarps * kGroupMax * 4 * 2 + kConsumerWarps * 4 + 15) / 16 * 16;
   static constexpr int kBarBytes = (2 * kStages + 2) * 8;
   static constexpr int kSmemBytes = kRingBytes + kMergeBytes + kMlBytes + kBarBytes + kStages * 4 + 64;
 };
@@ -260,43 +263,66 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
 
   if (warp == 0) {
     // ======================= producer warp =======================
+    // Stages are issued in batches, one lane per stage: each lane loads its
+    // tiles' page ids, waits for its stage to be free and issues the copies.
+    // A batch holds at most kStages stages, so it only waits on stages that an
+    // earlier batch filled.
     const uint64_t pol = l2_policy_evict_first();
     Cursor cur = start;
     Piece p;
-    uint32_t j = 0;
+    uint32_t j = 0;  // stages issued so far
     bool ok = true;
     while (ok && next_piece(cur, a, p)) {
       const int32_t* ptrow = a.page_table + static_cast<int64_t>(p.r) * a.max_pages;
-      for (int t = p.t0; t < p.t1 && ok; t += 32) {
-        const int cnt = min(32, p.t1 - t);
-        int pid = 0;
-        if (lane < cnt) pid = __ldg(ptrow + (t + lane) / tpp);
-        for (int i = 0; i < cnt; ++i) {
-          const int page = __shfl_sync(kFull, pid, i);
-          const uint32_t stage = j % C::kStages;
-          const uint32_t round = j / C::kStages;
-          if (lane == 0) {
-            if (round > 0) ok = mbar_wait(empty0 + 8 * stage, (round - 1) & 1, a.status);
-            if (ok) {
-              const uint32_t fb = full0 + 8 * stage;
-              if (page >= 0 && page < a.num_pages) {
-                const int sub = (t + i) % tpp;
-                const int64_t blk = (static_cast<int64_t>(page) * a.Hkv + p.h) * tpp + sub;
-                s_stage_fault[stage] = 0;
-                mbar_arrive_expect_tx(fb, C::kStageBytes);
-                const uint32_t dst = smem_addr(ring + stage * C::kStageBytes);
-                bulk_g2s(dst, a.k_pool + blk * C::kBlockBytes, C::kBlockBytes, fb, pol);
-                bulk_g2s(dst + C::kBlockBytes, a.v_pool + blk * C::kBlockBytes, C::kBlockBytes, fb, pol);
+      const int nst = (p.t1 - p.t0 + 1) >> 1;
+      for (int k0 = 0; k0 < nst; k0 += C::kStages) {
+        const int cnt = min(C::kStages, nst - k0);
+        bool lok = true;
+        if (lane < cnt) {
+          const int tA = p.t0 + 2 * (k0 + lane);
+          const bool hasB = tA + 1 < p.t1;
+          const int pgA = __ldg(ptrow + tA / tpp);
+          const int pgB = hasB ? __ldg(ptrow + (tA + 1) / tpp) : -1;
+          const uint32_t jj = j + lane;
+          const uint32_t stage = jj % C::kStages;
+          const uint32_t round = jj / C::kStages;
+          if (round > 0) lok = mbar_wait(empty0 + 8 * stage, (round - 1) & 1, a.status);
+          if (lok) {
+            const bool okA = pgA >= 0 && pgA < a.num_pages;
+            const bool okB = hasB && pgB >= 0 && pgB < a.num_pages;
+            const uint32_t fb = full0 + 8 * stage;
+            s_stage_fault[stage] = (okA ? 0 : 1) | ((hasB && !okB) ? 2 : 0);
+            const uint32_t bytes = (okA ? 2u * C::kBlockBytes : 0u) + (okB ? 2u * C::kBlockBytes : 0u);
+            if (bytes == 0) {
+              mbar_arrive(fb);
+            } else {
+              mbar_arrive_expect_tx(fb, bytes);
+              const uint32_t dst = smem_addr(ring + stage * C::kStageBytes);
+              const int64_t blkA = (static_cast<int64_t>(pgA) * a.Hkv + p.h) * tpp + tA % tpp;
+              if (okA && okB && tA / tpp == (tA + 1) / tpp) {
+                // both tiles in one page: their K blocks (and V blocks) are adjacent
+                bulk_g2s(dst, a.k_pool + blkA * C::kBlockBytes, 2 * C::kBlockBytes, fb, pol);
+                bulk_g2s(dst + 2 * C::kBlockBytes, a.v_pool + blkA * C::kBlockBytes, 2 * C::kBlockBytes,
+                         fb, pol);
               } else {
-                s_stage_fault[stage] = 1;
-                mbar_arrive(fb);
+                if (okA) {
+                  bulk_g2s(dst, a.k_pool + blkA * C::kBlockBytes, C::kBlockBytes, fb, pol);
+                  bulk_g2s(dst + 2 * C::kBlockBytes, a.v_pool + blkA * C::kBlockBytes, C::kBlockBytes,
+                           fb, pol);
+                }
+                if (okB) {
+                  const int64_t blkB = (static_cast<int64_t>(pgB) * a.Hkv + p.h) * tpp + (tA + 1) % tpp;
+                  bulk_g2s(dst + C::kBlockBytes, a.k_pool + blkB * C::kBlockBytes, C::kBlockBytes, fb, pol);
+                  bulk_g2s(dst + 3 * C::kBlockBytes, a.v_pool + blkB * C::kBlockBytes, C::kBlockBytes,
+                           fb, pol);
+                }
               }
             }
           }
-          ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          ++j;
         }
+        ok = __all_sync(kFull, lok);
+        if (!ok) break;
+        j += cnt;
       }
     }
     if (!ok && lane == 0) {
@@ -387,9 +413,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     int fault = 0;
+    const int nst = (ntiles + 1) >> 1;  // stages of this piece, two tiles each
 
-    for (int i = c; i < ntiles; i += kConsumerWarps) {
-      const uint32_t j = jbase + i;
+    for (int k = c; k < nst; k += kConsumerWarps) {
+      const uint32_t j = jbase + k;
       const uint32_t stage = j % C::kStages;
       const uint32_t round = j / C::kStages;
       const bool got = mbar_wait(full0 + 8 * stage, round & 1, a.status);
@@ -397,13 +424,19 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         ok = false;
         break;
       }
-      if (s_stage_fault[stage]) {
-        fault = 1;
-      } else {
-        const uint8_t* Ks = ring + stage * C::kStageBytes;
-        const uint8_t* Vs = Ks + C::kBlockBytes;
-        const int nvalid = min(kTile, L - (p.t0 + i) * kTile);
-        // ---- S^T = K Q^T  (rows: tokens, cols: heads)
+      const int fbits = s_stage_fault[stage];
+      fault |= fbits;
+      const uint8_t* Sb = ring + stage * C::kStageBytes;
+      const int tA = p.t0 + 2 * k;
+      // tokens of each tile that take part: 0 for a tile past the piece or on a bad page
+      int nv[2];
+      nv[0] = (fbits & 1) ? 0 : min(kTile, L - tA * kTile);
+      nv[1] = (tA + 1 >= p.t1 || (fbits & 2)) ? 0 : min(kTile, L - (tA + 1) * kTile);
+      // ---- S^T = K Q^T for both tiles (rows: tokens, cols: heads); four independent chains
+      float sc[2][4];
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const uint8_t* Ks = Sb + tt * C::kBlockBytes;
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
         if (kFp8) {
           const uint4 ka0 = lds128(Ks + rowA * kDim + 16 * t4);
@@ -437,63 +470,75 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
             else mma_bf16(acc0, af, qf[kk][0], qf[kk][1]);
           }
         }
-        float s0 = (acc0[0] + acc1[0]) * mult0;
-        float s1 = (acc0[1] + acc1[1]) * mult1;
-        float s2 = (acc0[2] + acc1[2]) * mult0;
-        float s3 = (acc0[3] + acc1[3]) * mult1;
-        if (nvalid < kTile) {
-          if (rowA >= nvalid) s0 = s1 = kNegInf;
-          if (rowA + 2 >= nvalid) s2 = s3 = kNegInf;
+        sc[tt][0] = (acc0[0] + acc1[0]) * mult0;
+        sc[tt][1] = (acc0[1] + acc1[1]) * mult1;
+        sc[tt][2] = (acc0[2] + acc1[2]) * mult0;
+        sc[tt][3] = (acc0[3] + acc1[3]) * mult1;
+        if (nv[tt] < kTile) {
+          // select, never multiply: a stale slot may hold NaN codes
+          if (rowA >= nv[tt]) sc[tt][0] = sc[tt][1] = kNegInf;
+          if (rowA + 2 >= nv[tt]) sc[tt][2] = sc[tt][3] = kNegInf;
         }
-        // ---- online softmax (log2 domain), per head over the tile's tokens
-        float tm0 = fmaxf(s0, s2), tm1 = fmaxf(s1, s3);
+      }
+      // ---- online softmax (log2 domain), per head over the stage's 32 tokens
+      float tm0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
+      float tm1 = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, off));
-          tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, off));
-        }
-        const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
-        if (__any_sync(kFull, mn0 > m0 || mn1 > m1)) {
-          const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+      for (int off = 4; off < 32; off <<= 1) {
+        tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, off));
+        tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, off));
+      }
+      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+      if (__any_sync(kFull, mn0 > m0 || mn1 > m1)) {
+        const float al0 = mn0 == m0 ? 1.f : fast_exp2(m0 - mn0);
+        const float al1 = mn1 == m1 ? 1.f : fast_exp2(m1 - mn1);
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-          }
-          l0 *= al0;
-          l1 *= al1;
-          m0 = mn0;
-          m1 = mn1;
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= al0;
+          o[mt][1] *= al1;
+          o[mt][2] *= al0;
+          o[mt][3] *= al1;
         }
-        const float p0 = fast_exp2(s0 - m0), p1 = fast_exp2(s1 - m1);
-        const float p2 = fast_exp2(s2 - m0), p3 = fast_exp2(s3 - m1);
+        l0 *= al0;
+        l1 *= al1;
+        m0 = mn0;
+        m1 = mn1;
+      }
+      const float base0 = m0 == kNegInf ? 0.f : m0, base1 = m1 == kNegInf ? 0.f : m1;
+      // ---- P^T as the B operand of O^T = V^T P^T, per tile
+      // (bf16 keeps only 8 significant bits, so the bf16 cache multiplies V by
+      // P = hi + lo, two bf16 parts; f16 P is exact enough for the FP8 cache)
+      uint32_t pb[2][2], pl[2][2];
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const float p0 = fast_exp2(sc[tt][0] - base0), p1 = fast_exp2(sc[tt][1] - base1);
+        const float p2 = fast_exp2(sc[tt][2] - base0), p3 = fast_exp2(sc[tt][3] - base1);
         l0 += p0 + p2;
         l1 += p1 + p3;
-        // ---- P^T as the B operand of O^T = V^T P^T
-        // (bf16 keeps only 8 significant bits, so the bf16 cache multiplies V by
-        // P = hi + lo, two bf16 parts; f16 P is exact enough for the FP8 cache)
         const uint32_t pr0 = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         const uint32_t pr1 = kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3);
-        const uint32_t pb0 = movmatrix_trans(pr0);
-        const uint32_t pb1 = movmatrix_trans(pr1);
-        uint32_t pl0 = 0, pl1 = 0;
+        pb[tt][0] = movmatrix_trans(pr0);
+        pb[tt][1] = movmatrix_trans(pr1);
+        pl[tt][0] = pl[tt][1] = 0u;
         if (!kFp8) {
-          pl0 = movmatrix_trans(pack_bf16x2(p0 - __uint_as_float(pr0 << 16),
-                                            p1 - __uint_as_float(pr0 & 0xffff0000u)));
-          pl1 = movmatrix_trans(pack_bf16x2(p2 - __uint_as_float(pr1 << 16),
-                                            p3 - __uint_as_float(pr1 & 0xffff0000u)));
+          pl[tt][0] = movmatrix_trans(pack_bf16x2(p0 - __uint_as_float(pr0 << 16),
+                                                  p1 - __uint_as_float(pr0 & 0xffff0000u)));
+          pl[tt][1] = movmatrix_trans(pack_bf16x2(p2 - __uint_as_float(pr1 << 16),
+                                                  p3 - __uint_as_float(pr1 & 0xffff0000u)));
         }
-        // mask for V columns past the context (stale slots may hold NaN codes)
-        const int nv = nvalid - 4 * t4;
+      }
+      // ---- O^T += V^T P^T (V columns past the context are zeroed: stale slots may hold NaN codes)
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const uint8_t* Vs = Sb + (2 + tt) * C::kBlockBytes;
+        const int nvt = nv[tt] - 4 * t4;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           if (kFp8) {
             uint32_t va = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g) * 16 + 4 * t4);
             uint32_t vb = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g + 8) * 16 + 4 * t4);
-            if (nv < 4) {
-              const uint32_t keep = nv <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nv)));
+            if (nvt < 4) {
+              const uint32_t keep = nvt <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvt)));
               va &= keep;
               vb &= keep;
             }
@@ -501,28 +546,28 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
                                     e4m3x2_to_f16x2(static_cast<uint16_t>(vb)),
                                     e4m3x2_to_f16x2(static_cast<uint16_t>(va >> 16)),
                                     e4m3x2_to_f16x2(static_cast<uint16_t>(vb >> 16))};
-            mma_f16(o[mt], af, pb0, pb1);
+            mma_f16(o[mt], af, pb[tt][0], pb[tt][1]);
           } else {
             uint2 va = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g) * 32 + 8 * t4);
             uint2 vb = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g + 8) * 32 + 8 * t4);
-            if (nv < 4) {
-              const uint32_t k0 = nv <= 0 ? 0u : nv == 1 ? 0x0000ffffu : 0xffffffffu;
-              const uint32_t k1 = nv <= 2 ? 0u : nv == 3 ? 0x0000ffffu : 0xffffffffu;
+            if (nvt < 4) {
+              const uint32_t k0 = nvt <= 0 ? 0u : nvt == 1 ? 0x0000ffffu : 0xffffffffu;
+              const uint32_t k1 = nvt <= 2 ? 0u : nvt == 3 ? 0x0000ffffu : 0xffffffffu;
               va.x &= k0;
               va.y &= k1;
               vb.x &= k0;
               vb.y &= k1;
             }
             const uint32_t af[4] = {va.x, vb.x, va.y, vb.y};
-            mma_bf16(o[mt], af, pb0, pb1);
-            mma_bf16(o[mt], af, pl0, pl1);
+            mma_bf16(o[mt], af, pb[tt][0], pb[tt][1]);
+            mma_bf16(o[mt], af, pl[tt][0], pl[tt][1]);
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * stage);
     }
-    jbase += ntiles;
+    jbase += nst;
     if (!ok) break;
 
     // ---- merge the consumer warps' (m, l, O) of this piece
