@@ -73,6 +73,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase's completion.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; false (and a status
 // bit) if it did not within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
@@ -141,6 +154,18 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Four e4m3 codes of one word (bytes b0..b3) to f16x2 pairs (b0, b1) -> lo and
+// (b2, b3) -> hi, exactly; one hardware conversion per pair, the word split
+// into its 16-bit halves inside the asm block (no repacking).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l16, h16;\n\t"
+      "mov.b32 {l16, h16}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l16;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h16;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Pack two fp32 into f16x2 / bf16x2 (round to nearest even; `lo` in the low half).

@@ -263,11 +263,19 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
 
   if (warp == 0) {
     // ======================= producer warp =======================
-    // Stages are issued in batches, one lane per stage: each lane loads its
-    // tiles' page ids, waits for its stage to be free and issues the copies.
-    // A batch holds at most kStages stages, so it only waits on stages that an
-    // earlier batch filled.
+    // Bulk copies issued by one thread complete one after another, so every
+    // copy gets its own lane: lanes 4s..4s+3 serve stage s of a batch of up
+    // to 8 stages (K and V of the stage's two tiles).  The group leader polls
+    // the stage's "empty" barrier and, once it is free, sets the stage's
+    // transaction count; after a warp sync the group's lanes issue their
+    // copies.  Stages are issued the moment they are free, so the ring never
+    // drains at a batch boundary, and a batch only waits on stages that an
+    // earlier batch filled.  Page ids of the next batch of the same piece are
+    // loaded while the current batch polls.
+    constexpr int kBatch = C::kStages < 8 ? C::kStages : 8;
     const uint64_t pol = l2_policy_evict_first();
+    const int si = lane >> 2;  // stage slot of this lane within a batch
+    const int ci = lane & 3;   // 0: K of tile A (or of both tiles), 1: V of A (or both), 2: K of B, 3: V of B
     Cursor cur = start;
     Piece p;
     uint32_t j = 0;  // stages issued so far
@@ -275,54 +283,81 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     while (ok && next_piece(cur, a, p)) {
       const int32_t* ptrow = a.page_table + static_cast<int64_t>(p.r) * a.max_pages;
       const int nst = (p.t1 - p.t0 + 1) >> 1;
-      for (int k0 = 0; k0 < nst; k0 += C::kStages) {
-        const int cnt = min(C::kStages, nst - k0);
-        bool lok = true;
-        if (lane < cnt) {
-          const int tA = p.t0 + 2 * (k0 + lane);
-          const bool hasB = tA + 1 < p.t1;
-          const int pgA = __ldg(ptrow + tA / tpp);
-          const int pgB = hasB ? __ldg(ptrow + (tA + 1) / tpp) : -1;
-          const uint32_t jj = j + lane;
-          const uint32_t stage = jj % C::kStages;
-          const uint32_t round = jj / C::kStages;
-          if (round > 0) lok = mbar_wait(empty0 + 8 * stage, (round - 1) & 1, a.status);
-          if (lok) {
-            const bool okA = pgA >= 0 && pgA < a.num_pages;
-            const bool okB = hasB && pgB >= 0 && pgB < a.num_pages;
-            const uint32_t fb = full0 + 8 * stage;
+      // page id of the tile this lane copies (tile A for ci < 2, B otherwise)
+      auto load_id = [&](int k0) {
+        int pg = -1;
+        if (si < kBatch && k0 + si < nst) {
+          const int t = p.t0 + 2 * (k0 + si) + (ci >> 1);
+          if (t < p.t1) pg = __ldg(ptrow + t / tpp);
+        }
+        return pg;
+      };
+      int pg = load_id(0);
+      for (int k0 = 0; k0 < nst && ok; k0 += kBatch) {
+        const int cnt = min(kBatch, nst - k0);
+        const int nxt = load_id(k0 + kBatch);  // prefetch (unused past the piece)
+        const bool member = si < cnt;
+        const int tA = p.t0 + 2 * (k0 + si);
+        const bool hasB = tA + 1 < p.t1;
+        const int pgA = __shfl_sync(kFull, pg, lane & ~3);
+        const int pgB = __shfl_sync(kFull, pg, (lane & ~3) | 2);
+        const bool okA = pgA >= 0 && pgA < a.num_pages;
+        const bool okB = hasB && pgB >= 0 && pgB < a.num_pages;
+        const bool pair = okA && okB && tA / tpp == (tA + 1) / tpp;  // adjacent blocks of one page
+        const uint32_t jj = j + si;
+        const uint32_t stage = jj % C::kStages;
+        const uint32_t round = jj / C::kStages;
+        const uint32_t fb = full0 + 8 * stage;
+        bool todo = member;
+        bool ready = false;
+        bool issued = false;
+        const uint64_t t0 = global_timer_ns();
+        uint32_t spins = 0;
+        while (__any_sync(kFull, todo)) {
+          if (todo && ci == 0 && !ready &&
+              (round == 0 || mbar_test(empty0 + 8 * stage, (round - 1) & 1))) {
+            ready = true;
             s_stage_fault[stage] = (okA ? 0 : 1) | ((hasB && !okB) ? 2 : 0);
             const uint32_t bytes = (okA ? 2u * C::kBlockBytes : 0u) + (okB ? 2u * C::kBlockBytes : 0u);
-            if (bytes == 0) {
-              mbar_arrive(fb);
-            } else {
-              mbar_arrive_expect_tx(fb, bytes);
-              const uint32_t dst = smem_addr(ring + stage * C::kStageBytes);
-              const int64_t blkA = (static_cast<int64_t>(pgA) * a.Hkv + p.h) * tpp + tA % tpp;
-              if (okA && okB && tA / tpp == (tA + 1) / tpp) {
-                // both tiles in one page: their K blocks (and V blocks) are adjacent
-                bulk_g2s(dst, a.k_pool + blkA * C::kBlockBytes, 2 * C::kBlockBytes, fb, pol);
-                bulk_g2s(dst + 2 * C::kBlockBytes, a.v_pool + blkA * C::kBlockBytes, 2 * C::kBlockBytes,
-                         fb, pol);
-              } else {
-                if (okA) {
-                  bulk_g2s(dst, a.k_pool + blkA * C::kBlockBytes, C::kBlockBytes, fb, pol);
-                  bulk_g2s(dst + 2 * C::kBlockBytes, a.v_pool + blkA * C::kBlockBytes, C::kBlockBytes,
-                           fb, pol);
-                }
-                if (okB) {
-                  const int64_t blkB = (static_cast<int64_t>(pgB) * a.Hkv + p.h) * tpp + (tA + 1) % tpp;
-                  bulk_g2s(dst + C::kBlockBytes, a.k_pool + blkB * C::kBlockBytes, C::kBlockBytes, fb, pol);
-                  bulk_g2s(dst + 3 * C::kBlockBytes, a.v_pool + blkB * C::kBlockBytes, C::kBlockBytes,
-                           fb, pol);
-                }
+            if (bytes == 0) mbar_arrive(fb);
+            else mbar_arrive_expect_tx(fb, bytes);
+          }
+          __syncwarp();
+          const bool go = __shfl_sync(kFull, ready, lane & ~3) && todo;
+          if (go) {
+            todo = false;
+            issued = true;
+            const uint32_t dst = smem_addr(ring + stage * C::kStageBytes);
+            const int tt = ci >> 1;  // tile of this lane's copy
+            const bool isV = ci & 1;
+            const uint8_t* pool = isV ? a.v_pool : a.k_pool;
+            const uint32_t slot = (isV ? 2u : 0u);
+            if (pair) {
+              if (tt == 0) {
+                const int64_t blk = (static_cast<int64_t>(pgA) * a.Hkv + p.h) * tpp + tA % tpp;
+                bulk_g2s(dst + slot * C::kBlockBytes, pool + blk * C::kBlockBytes, 2 * C::kBlockBytes, fb, pol);
               }
+            } else if (tt == 0 ? okA : okB) {
+              const int t = tA + tt;
+              const int64_t blk = (static_cast<int64_t>(tt == 0 ? pgA : pgB) * a.Hkv + p.h) * tpp + t % tpp;
+              bulk_g2s(dst + (slot + tt) * C::kBlockBytes, pool + blk * C::kBlockBytes, C::kBlockBytes, fb, pol);
             }
           }
+          // the give-up decision is taken by lane 0 for the whole warp
+          const bool late = (++spins & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs;
+          if (__shfl_sync(kFull, late, 0)) {
+            if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+            ok = false;
+            break;
+          }
         }
-        ok = __all_sync(kFull, lok);
-        if (!ok) break;
+        if (!ok) {
+          // this batch's copies that did go out must land before the CTA exits
+          if (issued && ci == 0) mbar_wait(fb, round & 1, a.status);
+          break;
+        }
         j += cnt;
+        pg = nxt;
       }
     }
     if (!ok && lane == 0) {
@@ -432,40 +467,54 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       int nv[2];
       nv[0] = (fbits & 1) ? 0 : min(kTile, L - tA * kTile);
       nv[1] = (tA + 1 >= p.t1 || (fbits & 2)) ? 0 : min(kTile, L - (tA + 1) * kTile);
+      // ---- FP8: copy this lane's K and V operands of both tiles to registers
+      // and hand the stage back at once, so the producer refills it while the
+      // math below runs (the bf16 operands are twice as large and stay in
+      // shared memory until the stage's math is done)
+      uint4 kr[2][4];
+      uint32_t vr[2][8][2];
+      if (kFp8) {
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+          const uint8_t* Ks = Sb + tt * C::kBlockBytes;
+          const uint8_t* Vs = Sb + (2 + tt) * C::kBlockBytes;
+          kr[tt][0] = lds128(Ks + rowA * kDim + 16 * t4);
+          kr[tt][1] = lds128(Ks + rowA * kDim + 64 + 16 * t4);
+          kr[tt][2] = lds128(Ks + (rowA + 2) * kDim + 16 * t4);
+          kr[tt][3] = lds128(Ks + (rowA + 2) * kDim + 64 + 16 * t4);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            vr[tt][mt][0] = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g) * 16 + 4 * t4);
+            vr[tt][mt][1] = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g + 8) * 16 + 4 * t4);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      }
       // ---- S^T = K Q^T for both tiles (rows: tokens, cols: heads); four independent chains
       float sc[2][4];
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
-        const uint8_t* Ks = Sb + tt * C::kBlockBytes;
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-        if (kFp8) {
-          const uint4 ka0 = lds128(Ks + rowA * kDim + 16 * t4);
-          const uint4 ka1 = lds128(Ks + rowA * kDim + 64 + 16 * t4);
-          const uint4 kb0 = lds128(Ks + (rowA + 2) * kDim + 16 * t4);
-          const uint4 kb1 = lds128(Ks + (rowA + 2) * kDim + 64 + 16 * t4);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t wa = word_of(kk < 4 ? ka0 : ka1, kk & 3);
-            const uint32_t wb = word_of(kk < 4 ? kb0 : kb1, kk & 3);
-            const uint32_t af[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(wa)),
-                                    e4m3x2_to_f16x2(static_cast<uint16_t>(wb)),
-                                    e4m3x2_to_f16x2(static_cast<uint16_t>(wa >> 16)),
-                                    e4m3x2_to_f16x2(static_cast<uint16_t>(wb >> 16))};
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t af[4];
+          if (kFp8) {
+            const uint32_t wa = word_of(kr[tt][kk >> 2], kk & 3);
+            const uint32_t wb = word_of(kr[tt][2 + (kk >> 2)], kk & 3);
+            e4m3x4_to_f16x4(wa, af[0], af[2]);
+            e4m3x4_to_f16x4(wb, af[1], af[3]);
             if (kk & 1) mma_f16(acc1, af, qf[kk][0], qf[kk][1]);
             else mma_f16(acc0, af, qf[kk][0], qf[kk][1]);
-          }
-        } else {
-          uint4 ka[4], kb[4];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            ka[cc] = lds128(Ks + rowA * 2 * kDim + 64 * cc + 16 * t4);
-            kb[cc] = lds128(Ks + (rowA + 2) * 2 * kDim + 64 * cc + 16 * t4);
-          }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          } else {
+            const uint8_t* Ks = Sb + tt * C::kBlockBytes;
             const int wi = 2 * (kk & 1);
-            const uint32_t af[4] = {word_of(ka[kk >> 1], wi), word_of(kb[kk >> 1], wi),
-                                    word_of(ka[kk >> 1], wi + 1), word_of(kb[kk >> 1], wi + 1)};
+            const uint4 ka = lds128(Ks + rowA * 2 * kDim + 64 * (kk >> 1) + 16 * t4);
+            const uint4 kb = lds128(Ks + (rowA + 2) * 2 * kDim + 64 * (kk >> 1) + 16 * t4);
+            af[0] = word_of(ka, wi);
+            af[1] = word_of(kb, wi);
+            af[2] = word_of(ka, wi + 1);
+            af[3] = word_of(kb, wi + 1);
             if (kk & 1) mma_bf16(acc1, af, qf[kk][0], qf[kk][1]);
             else mma_bf16(acc0, af, qf[kk][0], qf[kk][1]);
           }
@@ -530,42 +579,42 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       // ---- O^T += V^T P^T (V columns past the context are zeroed: stale slots may hold NaN codes)
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
-        const uint8_t* Vs = Sb + (2 + tt) * C::kBlockBytes;
         const int nvt = nv[tt] - 4 * t4;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           if (kFp8) {
-            uint32_t va = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g) * 16 + 4 * t4);
-            uint32_t vb = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g + 8) * 16 + 4 * t4);
+            uint32_t va = vr[tt][mt][0], vb = vr[tt][mt][1];
             if (nvt < 4) {
               const uint32_t keep = nvt <= 0 ? 0u : (0xffffffffu >> (8 * (4 - nvt)));
               va &= keep;
               vb &= keep;
             }
-            const uint32_t af[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(va)),
-                                    e4m3x2_to_f16x2(static_cast<uint16_t>(vb)),
-                                    e4m3x2_to_f16x2(static_cast<uint16_t>(va >> 16)),
-                                    e4m3x2_to_f16x2(static_cast<uint16_t>(vb >> 16))};
+            uint32_t af[4];
+            e4m3x4_to_f16x4(va, af[0], af[2]);
+            e4m3x4_to_f16x4(vb, af[1], af[3]);
             mma_f16(o[mt], af, pb[tt][0], pb[tt][1]);
           } else {
-            uint2 va = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g) * 32 + 8 * t4);
-            uint2 vb = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g + 8) * 32 + 8 * t4);
+            const uint8_t* Vs = Sb + (2 + tt) * C::kBlockBytes;
+            const uint2 va = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g) * 32 + 8 * t4);
+            const uint2 vb = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g + 8) * 32 + 8 * t4);
+            uint32_t af[4] = {va.x, vb.x, va.y, vb.y};
             if (nvt < 4) {
               const uint32_t k0 = nvt <= 0 ? 0u : nvt == 1 ? 0x0000ffffu : 0xffffffffu;
               const uint32_t k1 = nvt <= 2 ? 0u : nvt == 3 ? 0x0000ffffu : 0xffffffffu;
-              va.x &= k0;
-              va.y &= k1;
-              vb.x &= k0;
-              vb.y &= k1;
+              af[0] &= k0;
+              af[1] &= k0;
+              af[2] &= k1;
+              af[3] &= k1;
             }
-            const uint32_t af[4] = {va.x, vb.x, va.y, vb.y};
             mma_bf16(o[mt], af, pb[tt][0], pb[tt][1]);
             mma_bf16(o[mt], af, pl[tt][0], pl[tt][1]);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      if (!kFp8) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      }
     }
     jbase += nst;
     if (!ok) break;
