@@ -168,17 +168,16 @@ def oracle_segment_problem(wl, r: int, h: int, step: int):
     ps, D, G = wl.page_size, wl.D, wl.G
     P = -(-L // ps)
     a, b = int(wl.cu_prompt[r]), int(wl.cu_prompt[r + 1])
-    kp = np.full(P * ps * D, 0x7F, np.uint8)
-    vp = np.full(P * ps * D, 0x7F, np.uint8)
+    kv = np.full(2 * P * ps * D, 0x7F, np.uint8)
     pt = np.arange(P, dtype=np.int32)[None, :]
     k = np.ascontiguousarray(wl.k_prompt[a:b, h:h + 1])
     v = np.ascontiguousarray(wl.v_prompt[a:b, h:h + 1])
-    oracle.kv_prefill(k, v, np.array([0, b - a], np.int32), kp, vp, wl.k_scale, wl.v_scale, pt,
+    oracle.kv_prefill(k, v, np.array([0, b - a], np.int32), kv, wl.k_scale, wl.v_scale, pt,
                       None, None, None, fp8=True, Hkv=1, D=D, page_size=ps, num_pages=P)
     kn, vn = wl.step_tokens(step)
     q = np.ascontiguousarray(wl.step_query(step)[r:r + 1, h * G:(h + 1) * G])
     return dict(kn=np.ascontiguousarray(kn[r:r + 1, h:h + 1]), vn=np.ascontiguousarray(vn[r:r + 1, h:h + 1]),
-                kp=kp, vp=vp, pt=pt, lens=np.array([L], np.int32), q=q, P=P,
+                kv=kv, pt=pt, lens=np.array([L], np.int32), q=q, P=P,
                 tags=np.zeros(P, np.uint32), exp=np.zeros((1, P), np.uint32))
 
 
@@ -186,12 +185,12 @@ def oracle_segment_step(wl, prob) -> None:
     """The oracle's decode step on one segment: append, tag check, fp64 attention."""
     import oracle
     ps = wl.page_size
-    oracle.kv_append(prob["kn"], prob["vn"], prob["kp"], prob["vp"], wl.k_scale, wl.v_scale,
+    oracle.kv_append(prob["kn"], prob["vn"], prob["kv"], wl.k_scale, wl.v_scale,
                      prob["pt"], prob["lens"], prob["tags"], prob["exp"], None, fp8=True, Hkv=1,
                      D=wl.D, page_size=ps, num_pages=prob["P"])
     mask, _ = oracle.page_tags_validate(prob["pt"], prob["exp"], prob["lens"], prob["tags"],
                                         prob["P"], ps)
-    oracle.paged_attention(prob["q"], prob["kp"], prob["vp"], prob["pt"], prob["lens"], fp8=True,
+    oracle.paged_attention(prob["q"], prob["kv"], prob["pt"], prob["lens"], fp8=True,
                            k_scale=wl.k_scale, v_scale=wl.v_scale, abort_mask=mask,
                            sm_scale=wl.sm_scale, Hkv=1, page_size=ps, num_pages=prob["P"])
 

@@ -34,24 +34,24 @@ _SZ = ctypes.c_size_t
 SIGNATURES = {
     "fpk_version": (ctypes.c_int, []),
     "fpk_status_str": (ctypes.c_char_p, [ctypes.c_int]),
-    "fpk_kv_append_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P,
+    "fpk_kv_append_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P,
                                          _I32, _I32, _I32, _I32, _I32, _P]),
-    "fpk_kv_append_bf16": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P,
+    "fpk_kv_append_bf16": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P,
                                           _I32, _I32, _I32, _I32, _I32, _P]),
-    "fpk_kv_prefill_fp8": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _P, _P,
+    "fpk_kv_prefill_fp8": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _P, _I32, _P, _P, _P,
                                           _I32, _I32, _I32, _I32, _I32, _P]),
-    "fpk_kv_prefill_bf16": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _I32, _P, _P, _P,
+    "fpk_kv_prefill_bf16": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _P, _P, _P,
                                            _I32, _I32, _I32, _I32, _I32, _P]),
     "fpk_quantize_e4m3": (ctypes.c_int, [_P, _P, _P, _I64, _P]),
     "fpk_page_tags_bump": (ctypes.c_int, [_P, _P, _I32, _I32, _P]),
     "fpk_page_tags_validate": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I32, _P, _P, _P]),
     "fpk_decode_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
-    "fpk_paged_decode_attn_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
+    "fpk_paged_decode_attn_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
                                                  _SZ, _I32, _F, _I32, _I32, _I32, _I32, _I32, _I32,
                                                  _P]),
-    "fpk_paged_decode_attn_bf16": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ,
+    "fpk_paged_decode_attn_bf16": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ,
                                                   _I32, _F, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
-    "fpk_paged_decode_attn_fp8_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _P, _P,
+    "fpk_paged_decode_attn_fp8_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P,
                                                          _P, _I32, _F, _I32, _I32, _I32, _I32, _I32,
                                                          _I32, _P]),
     "fpk_decode_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
@@ -122,13 +122,13 @@ def version() -> int:
     return load_library().fpk_version()
 
 
-def fpk_kv_append_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens,
+def fpk_kv_append_fp8(k_new, v_new, kv_pool, k_scale, v_scale, page_table, seq_lens,
                       live_tags=None, expected_tags=None, abort_mask=None, *, Hkv, D, page_size,
                       num_pages, stream=None):
     B, max_pages = page_table.shape
     _check(load_library().fpk_kv_append_fp8(
         _ptr(k_new, _BF16_LIKE, "k_new"), _ptr(v_new, _BF16_LIKE, "v_new"),
-        _ptr(k_pool, _U8, "k_pool"), _ptr(v_pool, _U8, "v_pool"),
+        _ptr(kv_pool, _U8, "kv_pool"),
         _ptr(k_scale, _F32, "k_scale"), _ptr(v_scale, _F32, "v_scale"),
         _ptr(page_table, _I32T, "page_table"), max_pages, _ptr(seq_lens, _I32T, "seq_lens"),
         _ptr(live_tags, _TAGS, "live_tags", True), _ptr(expected_tags, _TAGS, "expected_tags", True),
@@ -136,26 +136,26 @@ def fpk_kv_append_fp8(k_new, v_new, k_pool, v_pool, k_scale, v_scale, page_table
         _stream(stream)), "fpk_kv_append_fp8")
 
 
-def fpk_kv_append_bf16(k_new, v_new, k_pool, v_pool, page_table, seq_lens, live_tags=None,
+def fpk_kv_append_bf16(k_new, v_new, kv_pool, page_table, seq_lens, live_tags=None,
                        expected_tags=None, abort_mask=None, *, Hkv, D, page_size, num_pages,
                        stream=None):
     B, max_pages = page_table.shape
     _check(load_library().fpk_kv_append_bf16(
         _ptr(k_new, _BF16_LIKE, "k_new"), _ptr(v_new, _BF16_LIKE, "v_new"),
-        _ptr(k_pool, _BF16_LIKE, "k_pool"), _ptr(v_pool, _BF16_LIKE, "v_pool"),
+        _ptr(kv_pool, _BF16_LIKE, "kv_pool"),
         _ptr(page_table, _I32T, "page_table"), max_pages, _ptr(seq_lens, _I32T, "seq_lens"),
         _ptr(live_tags, _TAGS, "live_tags", True), _ptr(expected_tags, _TAGS, "expected_tags", True),
         _ptr(abort_mask, _U8, "abort_mask", True), B, Hkv, D, page_size, num_pages,
         _stream(stream)), "fpk_kv_append_bf16")
 
 
-def fpk_kv_prefill_fp8(k, v, cu_seqlens, k_pool, v_pool, k_scale, v_scale, page_table,
+def fpk_kv_prefill_fp8(k, v, cu_seqlens, kv_pool, k_scale, v_scale, page_table,
                        live_tags=None, expected_tags=None, abort_mask=None, *, Hkv, D, page_size,
                        num_pages, stream=None):
     B, max_pages = page_table.shape
     _check(load_library().fpk_kv_prefill_fp8(
         _ptr(k, _BF16_LIKE, "k"), _ptr(v, _BF16_LIKE, "v"), _ptr(cu_seqlens, _I32T, "cu_seqlens"),
-        k.shape[0], _ptr(k_pool, _U8, "k_pool"), _ptr(v_pool, _U8, "v_pool"),
+        k.shape[0], _ptr(kv_pool, _U8, "kv_pool"),
         _ptr(k_scale, _F32, "k_scale"), _ptr(v_scale, _F32, "v_scale"),
         _ptr(page_table, _I32T, "page_table"), max_pages,
         _ptr(live_tags, _TAGS, "live_tags", True), _ptr(expected_tags, _TAGS, "expected_tags", True),
@@ -163,13 +163,13 @@ def fpk_kv_prefill_fp8(k, v, cu_seqlens, k_pool, v_pool, k_scale, v_scale, page_
         _stream(stream)), "fpk_kv_prefill_fp8")
 
 
-def fpk_kv_prefill_bf16(k, v, cu_seqlens, k_pool, v_pool, page_table, live_tags=None,
+def fpk_kv_prefill_bf16(k, v, cu_seqlens, kv_pool, page_table, live_tags=None,
                         expected_tags=None, abort_mask=None, *, Hkv, D, page_size, num_pages,
                         stream=None):
     B, max_pages = page_table.shape
     _check(load_library().fpk_kv_prefill_bf16(
         _ptr(k, _BF16_LIKE, "k"), _ptr(v, _BF16_LIKE, "v"), _ptr(cu_seqlens, _I32T, "cu_seqlens"),
-        k.shape[0], _ptr(k_pool, _BF16_LIKE, "k_pool"), _ptr(v_pool, _BF16_LIKE, "v_pool"),
+        k.shape[0], _ptr(kv_pool, _BF16_LIKE, "kv_pool"),
         _ptr(page_table, _I32T, "page_table"), max_pages,
         _ptr(live_tags, _TAGS, "live_tags", True), _ptr(expected_tags, _TAGS, "expected_tags", True),
         _ptr(abort_mask, _U8, "abort_mask", True), B, Hkv, D, page_size, num_pages,
@@ -205,12 +205,12 @@ def fpk_decode_workspace_bytes(B, Hq, Hkv, D=128, num_splits=0) -> int:
     return int(n)
 
 
-def fpk_paged_decode_attn_fp8(q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens,
+def fpk_paged_decode_attn_fp8(q, kv_pool, k_scale, v_scale, page_table, seq_lens,
                               abort_mask, out, lse, workspace, *, Hkv, page_size, num_pages,
                               sm_scale, num_splits=0, stream=None):
     B, Hq, D = q.shape
     _check(load_library().fpk_paged_decode_attn_fp8(
-        _ptr(q, _BF16_LIKE, "q"), _ptr(k_pool, _U8, "k_pool"), _ptr(v_pool, _U8, "v_pool"),
+        _ptr(q, _BF16_LIKE, "q"), _ptr(kv_pool, _U8, "kv_pool"),
         _ptr(k_scale, _F32, "k_scale"), _ptr(v_scale, _F32, "v_scale"),
         _ptr(page_table, _I32T, "page_table"), page_table.shape[1], _ptr(seq_lens, _I32T, "seq_lens"),
         _ptr(abort_mask, _U8, "abort_mask", True), _ptr(out, _F32, "out"),
@@ -219,13 +219,13 @@ def fpk_paged_decode_attn_fp8(q, k_pool, v_pool, k_scale, v_scale, page_table, s
         _stream(stream)), "fpk_paged_decode_attn_fp8")
 
 
-def fpk_paged_decode_attn_bf16(q, k_pool, v_pool, page_table, seq_lens, abort_mask, out, lse,
+def fpk_paged_decode_attn_bf16(q, kv_pool, page_table, seq_lens, abort_mask, out, lse,
                                workspace, *, Hkv, page_size, num_pages, sm_scale, num_splits=0,
                                stream=None):
     B, Hq, D = q.shape
     _check(load_library().fpk_paged_decode_attn_bf16(
-        _ptr(q, _BF16_LIKE, "q"), _ptr(k_pool, _BF16_LIKE, "k_pool"),
-        _ptr(v_pool, _BF16_LIKE, "v_pool"), _ptr(page_table, _I32T, "page_table"),
+        _ptr(q, _BF16_LIKE, "q"), _ptr(kv_pool, _BF16_LIKE, "kv_pool"),
+        _ptr(page_table, _I32T, "page_table"),
         page_table.shape[1], _ptr(seq_lens, _I32T, "seq_lens"),
         _ptr(abort_mask, _U8, "abort_mask", True), _ptr(out, _F32, "out"),
         _ptr(lse, _F32, "lse", True), _ptr(workspace, _U8, "workspace"),
@@ -233,7 +233,7 @@ def fpk_paged_decode_attn_bf16(q, k_pool, v_pool, page_table, seq_lens, abort_ma
         _stream(stream)), "fpk_paged_decode_attn_bf16")
 
 
-def fpk_paged_decode_attn_fp8_noalloc(q, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens,
+def fpk_paged_decode_attn_fp8_noalloc(q, kv_pool, k_scale, v_scale, page_table, seq_lens,
                                       abort_mask, out, lse, *, Hkv, page_size, num_pages, sm_scale,
                                       num_splits=0, stream=None):
     """FP8 decode attention without a caller workspace, for callers that cannot
@@ -242,7 +242,7 @@ def fpk_paged_decode_attn_fp8_noalloc(q, k_pool, v_pool, k_scale, v_scale, page_
     on the GPU share that scratch and race."""
     B, Hq, D = q.shape
     _check(load_library().fpk_paged_decode_attn_fp8_noalloc(
-        _ptr(q, _BF16_LIKE, "q"), _ptr(k_pool, _U8, "k_pool"), _ptr(v_pool, _U8, "v_pool"),
+        _ptr(q, _BF16_LIKE, "q"), _ptr(kv_pool, _U8, "kv_pool"),
         _ptr(k_scale, _F32, "k_scale"), _ptr(v_scale, _F32, "v_scale"),
         _ptr(page_table, _I32T, "page_table"), page_table.shape[1], _ptr(seq_lens, _I32T, "seq_lens"),
         _ptr(abort_mask, _U8, "abort_mask", True), _ptr(out, _F32, "out"),

@@ -12,12 +12,12 @@
 //   list of 16-token tiles; the grid's W CTAs take equal contiguous ranges of
 //   it (one wave with the automatic W), so variable context lengths cost no
 //   tail.  A CTA finds its start with a block scan over seq_lens.
-// * Data movement.  Warp 0 is a producer: it reads page ids 32 at a time and
-//   one lane issues cp.async.bulk (TMA) copies of each tile's K block
-//   [16 tok][128] and V block [128][16 tok] -- both contiguous in the pool
-//   layout -- into a ring of shared-memory stages completing on mbarriers,
-//   with an L2 evict-first hint.  Page ids outside the pool are never
-//   dereferenced.
+// * Data movement.  Warp 0 is a producer: each of its lanes issues one
+//   cp.async.bulk (TMA) copy of one tile's K block [16 tok][128] and V block
+//   [128][16 tok] -- adjacent in the pool layout, so one copy of 4 KiB (FP8),
+//   or 8 KiB for two adjacent tiles of one page -- into a ring of shared-memory
+//   stages completing on mbarriers, with an L2 evict-first hint.  Page ids
+//   outside the pool are never dereferenced.
 // * Math.  Consumer warps take ring stages round-robin.  With the GQA group on
 //   the N side of the tensor-core tile, S^T = K Q^T and O^T = V^T P^T are
 //   m16n8k16 MMAs; e4m3 codes convert exactly to f16 in registers (the query
@@ -54,7 +54,8 @@ template <bool kFp8>
 struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kBlockBytes = kTile * kDim * kElem;  // one K (or V) tile
-  // a stage holds two consecutive tiles: [K tile 0][K tile 1][V tile 0][V tile 1]
+  // a stage holds two consecutive tiles, each as it lies in the pool:
+  // [K tile 0][V tile 0][K tile 1][V tile 1]
   static constexpr int kStageBytes = 4 * kBlockBytes;
   static constexpr int kStages = kFp8 ? 8 : 4;
   // Within a segment piece consumer warp c takes stages c, c+4, ...; with
@@ -74,8 +75,7 @@ struct Cfg {
 
 struct AttnArgs {
   const uint16_t* q;
-  const uint8_t* k_pool;
-  const uint8_t* v_pool;
+  const uint8_t* kv_pool;
   const float* k_scale;
   const float* v_scale;
   const int32_t* page_table;
@@ -264,18 +264,18 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   if (warp == 0) {
     // ======================= producer warp =======================
     // Bulk copies issued by one thread complete one after another, so every
-    // copy gets its own lane: lanes 4s..4s+3 serve stage s of a batch of up
-    // to 8 stages (K and V of the stage's two tiles).  The group leader polls
-    // the stage's "empty" barrier and, once it is free, sets the stage's
-    // transaction count; after a warp sync the group's lanes issue their
-    // copies.  Stages are issued the moment they are free, so the ring never
-    // drains at a batch boundary, and a batch only waits on stages that an
-    // earlier batch filled.  Page ids of the next batch of the same piece are
-    // loaded while the current batch polls.
-    constexpr int kBatch = C::kStages < 8 ? C::kStages : 8;
+    // copy gets its own lane: lanes 2s and 2s+1 serve stage s of a batch of
+    // up to 16 stages, one tile each (a tile's K and V blocks are adjacent in
+    // the pool: one copy); two adjacent tiles of one page go as one copy.  The
+    // even lane polls the stage's "empty" barrier and, once it is free, sets
+    // the stage's transaction count; after a warp sync both lanes issue.
+    // Stages are issued the moment they are free, so the ring never drains at
+    // a batch boundary, and a batch only waits on stages that an earlier batch
+    // filled.  Page ids of the next batch of a piece load while this one polls.
+    constexpr int kBatch = C::kStages < 16 ? C::kStages : 16;
     const uint64_t pol = l2_policy_evict_first();
-    const int si = lane >> 2;  // stage slot of this lane within a batch
-    const int ci = lane & 3;   // 0: K of tile A (or of both tiles), 1: V of A (or both), 2: K of B, 3: V of B
+    const int si = lane >> 1;  // stage slot of this lane within a batch
+    const int ci = lane & 1;   // tile of the stage this lane copies
     Cursor cur = start;
     Piece p;
     uint32_t j = 0;  // stages issued so far
@@ -283,11 +283,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     while (ok && next_piece(cur, a, p)) {
       const int32_t* ptrow = a.page_table + static_cast<int64_t>(p.r) * a.max_pages;
       const int nst = (p.t1 - p.t0 + 1) >> 1;
-      // page id of the tile this lane copies (tile A for ci < 2, B otherwise)
       auto load_id = [&](int k0) {
         int pg = -1;
         if (si < kBatch && k0 + si < nst) {
-          const int t = p.t0 + 2 * (k0 + si) + (ci >> 1);
+          const int t = p.t0 + 2 * (k0 + si) + ci;
           if (t < p.t1) pg = __ldg(ptrow + t / tpp);
         }
         return pg;
@@ -299,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         const bool member = si < cnt;
         const int tA = p.t0 + 2 * (k0 + si);
         const bool hasB = tA + 1 < p.t1;
-        const int pgA = __shfl_sync(kFull, pg, lane & ~3);
-        const int pgB = __shfl_sync(kFull, pg, (lane & ~3) | 2);
+        const int pgA = __shfl_sync(kFull, pg, lane & ~1);
+        const int pgB = __shfl_sync(kFull, pg, lane | 1);
         const bool okA = pgA >= 0 && pgA < a.num_pages;
         const bool okB = hasB && pgB >= 0 && pgB < a.num_pages;
-        const bool pair = okA && okB && tA / tpp == (tA + 1) / tpp;  // adjacent blocks of one page
+        const bool pair = okA && okB && tA / tpp == (tA + 1) / tpp;  // adjacent tiles of one page
         const uint32_t jj = j + si;
         const uint32_t stage = jj % C::kStages;
         const uint32_t round = jj / C::kStages;
@@ -323,24 +322,18 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
             else mbar_arrive_expect_tx(fb, bytes);
           }
           __syncwarp();
-          const bool go = __shfl_sync(kFull, ready, lane & ~3) && todo;
+          const bool go = __shfl_sync(kFull, ready, lane & ~1) && todo;
           if (go) {
             todo = false;
             issued = true;
-            const uint32_t dst = smem_addr(ring + stage * C::kStageBytes);
-            const int tt = ci >> 1;  // tile of this lane's copy
-            const bool isV = ci & 1;
-            const uint8_t* pool = isV ? a.v_pool : a.k_pool;
-            const uint32_t slot = (isV ? 2u : 0u);
+            const uint32_t dst = smem_addr(ring + stage * C::kStageBytes) + ci * 2 * C::kBlockBytes;
+            const int t = tA + ci;
+            const int64_t blk = (static_cast<int64_t>(ci == 0 ? pgA : pgB) * a.Hkv + p.h) * tpp + t % tpp;
+            const uint8_t* src = a.kv_pool + blk * 2 * C::kBlockBytes;
             if (pair) {
-              if (tt == 0) {
-                const int64_t blk = (static_cast<int64_t>(pgA) * a.Hkv + p.h) * tpp + tA % tpp;
-                bulk_g2s(dst + slot * C::kBlockBytes, pool + blk * C::kBlockBytes, 2 * C::kBlockBytes, fb, pol);
-              }
-            } else if (tt == 0 ? okA : okB) {
-              const int t = tA + tt;
-              const int64_t blk = (static_cast<int64_t>(tt == 0 ? pgA : pgB) * a.Hkv + p.h) * tpp + t % tpp;
-              bulk_g2s(dst + (slot + tt) * C::kBlockBytes, pool + blk * C::kBlockBytes, C::kBlockBytes, fb, pol);
+              if (ci == 0) bulk_g2s(dst, src, 4 * C::kBlockBytes, fb, pol);
+            } else if (ci == 0 ? okA : okB) {
+              bulk_g2s(dst, src, 2 * C::kBlockBytes, fb, pol);
             }
           }
           // the give-up decision is taken by lane 0 for the whole warp
@@ -461,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       }
       const int fbits = s_stage_fault[stage];
       fault |= fbits;
-      const uint8_t* Sb = ring + stage * C::kStageBytes;
+      const uint8_t* Sb = ring + stage * C::kStageBytes;  // [K0][V0][K1][V1]
       const int tA = p.t0 + 2 * k;
       // tokens of each tile that take part: 0 for a tile past the piece or on a bad page
       int nv[2];
@@ -476,8 +469,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       if (kFp8) {
 #pragma unroll
         for (int tt = 0; tt < 2; ++tt) {
-          const uint8_t* Ks = Sb + tt * C::kBlockBytes;
-          const uint8_t* Vs = Sb + (2 + tt) * C::kBlockBytes;
+          const uint8_t* Ks = Sb + 2 * tt * C::kBlockBytes;
+          const uint8_t* Vs = Ks + C::kBlockBytes;
           kr[tt][0] = lds128(Ks + rowA * kDim + 16 * t4);
           kr[tt][1] = lds128(Ks + rowA * kDim + 64 + 16 * t4);
           kr[tt][2] = lds128(Ks + (rowA + 2) * kDim + 16 * t4);
@@ -507,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
             if (kk & 1) mma_f16(acc1, af, qf[kk][0], qf[kk][1]);
             else mma_f16(acc0, af, qf[kk][0], qf[kk][1]);
           } else {
-            const uint8_t* Ks = Sb + tt * C::kBlockBytes;
+            const uint8_t* Ks = Sb + 2 * tt * C::kBlockBytes;
             const int wi = 2 * (kk & 1);
             const uint4 ka = lds128(Ks + rowA * 2 * kDim + 64 * (kk >> 1) + 16 * t4);
             const uint4 kb = lds128(Ks + (rowA + 2) * 2 * kDim + 64 * (kk >> 1) + 16 * t4);
@@ -594,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
             e4m3x4_to_f16x4(vb, af[1], af[3]);
             mma_f16(o[mt], af, pb[tt][0], pb[tt][1]);
           } else {
-            const uint8_t* Vs = Sb + (2 + tt) * C::kBlockBytes;
+            const uint8_t* Vs = Sb + (2 * tt + 1) * C::kBlockBytes;
             const uint2 va = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g) * 32 + 8 * t4);
             const uint2 vb = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g + 8) * 32 + 8 * t4);
             uint32_t af[4] = {va.x, vb.x, va.y, vb.y};
@@ -797,7 +790,7 @@ int check_attn_shapes(int B, int Hq, int Hkv, int D, int page_size, int num_page
 }
 
 template <bool kFp8>
-int attn_entry(const void* q, const void* k_pool, const void* v_pool, const float* k_scale,
+int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
                const float* v_scale, const int32_t* page_table, int32_t max_pages,
                const int32_t* seq_lens, const uint8_t* abort_mask, float* out, float* lse,
                void* workspace, size_t workspace_bytes, int32_t num_splits, float sm_scale,
@@ -806,9 +799,9 @@ int attn_entry(const void* q, const void* k_pool, const void* v_pool, const floa
   int st = check_attn_shapes(B, Hq, Hkv, D, page_size, num_pages, max_pages, num_splits);
   if (st != FPK_OK) return st;
   if (B == 0) return FPK_OK;
-  if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out || !workspace) return FPK_EINVAL;
+  if (!q || !kv_pool || !page_table || !seq_lens || !out || !workspace) return FPK_EINVAL;
   if (kFp8 && (!k_scale || !v_scale)) return FPK_EINVAL;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+  if (!aligned16(q) || !aligned16(kv_pool) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return FPK_EINVAL;
   int dev = 0;
@@ -825,8 +818,7 @@ int attn_entry(const void* q, const void* k_pool, const void* v_pool, const floa
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   AttnArgs a;
   a.q = static_cast<const uint16_t*>(q);
-  a.k_pool = static_cast<const uint8_t*>(k_pool);
-  a.v_pool = static_cast<const uint8_t*>(v_pool);
+  a.kv_pool = static_cast<const uint8_t*>(kv_pool);
   a.k_scale = k_scale;
   a.v_scale = v_scale;
   a.page_table = page_table;
@@ -868,7 +860,7 @@ extern "C" size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv,
   return fpk::layout(B, Hkv, Hq / Hkv, W).total;
 }
 
-extern "C" int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+extern "C" int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* kv_pool,
                                          const float* k_scale, const float* v_scale,
                                          const int32_t* page_table, int32_t max_pages,
                                          const int32_t* seq_lens, const uint8_t* abort_mask,
@@ -877,12 +869,12 @@ extern "C" int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* k_pool, c
                                          float sm_scale, int32_t B, int32_t Hq, int32_t Hkv,
                                          int32_t D, int32_t page_size, int32_t num_pages,
                                          void* stream) {
-  return fpk::attn_entry<true>(q, k_pool, v_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
+  return fpk::attn_entry<true>(q, kv_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
                                abort_mask, out, lse, workspace, workspace_bytes, num_splits,
                                sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream);
 }
 
-extern "C" int fpk_paged_decode_attn_bf16(const void* q, const void* k_pool, const void* v_pool,
+extern "C" int fpk_paged_decode_attn_bf16(const void* q, const void* kv_pool,
                                           const int32_t* page_table, int32_t max_pages,
                                           const int32_t* seq_lens, const uint8_t* abort_mask,
                                           float* out, float* lse, void* workspace,
@@ -890,7 +882,7 @@ extern "C" int fpk_paged_decode_attn_bf16(const void* q, const void* k_pool, con
                                           float sm_scale, int32_t B, int32_t Hq, int32_t Hkv,
                                           int32_t D, int32_t page_size, int32_t num_pages,
                                           void* stream) {
-  return fpk::attn_entry<false>(q, k_pool, v_pool, nullptr, nullptr, page_table, max_pages, seq_lens,
+  return fpk::attn_entry<false>(q, kv_pool, nullptr, nullptr, page_table, max_pages, seq_lens,
                                 abort_mask, out, lse, workspace, workspace_bytes, num_splits,
                                 sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream);
 }
@@ -944,8 +936,8 @@ int noalloc_scratch_address(int dev, void** addr) {
 }  // namespace
 }  // namespace fpk
 
-extern "C" int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k_pool,
-                                                 const uint8_t* v_pool, const float* k_scale,
+extern "C" int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* kv_pool,
+                                                 const float* k_scale,
                                                  const float* v_scale, const int32_t* page_table,
                                                  int32_t max_pages, const int32_t* seq_lens,
                                                  const uint8_t* abort_mask, float* out, float* lse,
@@ -973,7 +965,7 @@ extern "C" int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k
   // the status word and the arrival counters must start at zero
   if (cudaMemsetAsync(scratch, 0, l.part_ml, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FPK_ECUDA;
-  return fpk::attn_entry<true>(q, k_pool, v_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
+  return fpk::attn_entry<true>(q, kv_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
                                abort_mask, out, lse, scratch, fpk::kNoAllocScratchBytes, W, sm_scale,
                                B, Hq, Hkv, D, page_size, num_pages, stream);
 }

@@ -10,7 +10,8 @@
 //
 // One thread handles 8 consecutive dims of one (token, kv head): a 16-byte
 // bf16 load per tensor, an 8-byte (fp8) or 16-byte (bf16) store into the
-// token-major K row, and 8 strided element stores into the V column block.
+// token-major K block of the token's 16-token tile, and 8 strided element
+// stores into the tile's dim-major V block.
 #include "common.cuh"
 
 namespace fpk {
@@ -21,8 +22,7 @@ struct WriteArgs {
   const uint16_t* v_src;
   const int32_t* seq_lens;   // decode mode: position = seq_lens[r] - 1, row r
   const int32_t* cu_seqlens; // prefill mode: row i of request r at position i - cu[r]
-  uint8_t* k_pool;
-  uint8_t* v_pool;
+  uint8_t* kv_pool;
   const float* k_scale;
   const float* v_scale;
   const int32_t* page_table;
@@ -81,9 +81,11 @@ __global__ void __launch_bounds__(256) write_tokens_kernel(WriteArgs a) {
     const int64_t src = (row * a.Hkv + h) * a.D + 8 * c;
     const uint4 kraw = __ldg(reinterpret_cast<const uint4*>(a.k_src + src));
     const uint4 vraw = __ldg(reinterpret_cast<const uint4*>(a.v_src + src));
-    const int64_t kdst = ((static_cast<int64_t>(page) * a.Hkv + h) * a.page_size + off) * a.D + 8 * c;
-    const int64_t vblk = ((static_cast<int64_t>(page) * a.Hkv + h) * (a.page_size >> 4) + (off >> 4)) *
-                         a.D * 16;
+    // the token's 16-token tile: K block [16][D], then V block [D][16]
+    const int64_t tile = ((static_cast<int64_t>(page) * a.Hkv + h) * (a.page_size >> 4) + (off >> 4)) *
+                         2 * 16 * a.D;
+    const int64_t kdst = tile + (off & 15) * a.D + 8 * c;
+    const int64_t vblk = tile + 16 * a.D;
     const int vcol = off & 15;
     const uint16_t* kb = reinterpret_cast<const uint16_t*>(&kraw);
     const uint16_t* vb = reinterpret_cast<const uint16_t*>(&vraw);
@@ -102,12 +104,12 @@ __global__ void __launch_bounds__(256) write_tokens_kernel(WriteArgs a) {
         vq[2 * i] = static_cast<uint8_t>(vp & 0xFF);
         vq[2 * i + 1] = static_cast<uint8_t>(vp >> 8);
       }
-      *reinterpret_cast<uint2*>(a.k_pool + kdst) = make_uint2(kw[0], kw[1]);
+      *reinterpret_cast<uint2*>(a.kv_pool + kdst) = make_uint2(kw[0], kw[1]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a.v_pool[vblk + static_cast<int64_t>(8 * c + i) * 16 + vcol] = vq[i];
+      for (int i = 0; i < 8; ++i) a.kv_pool[vblk + static_cast<int64_t>(8 * c + i) * 16 + vcol] = vq[i];
     } else {
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.k_pool) + kdst) = kraw;
-      uint16_t* vpool = reinterpret_cast<uint16_t*>(a.v_pool);
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.kv_pool) + kdst) = kraw;
+      uint16_t* vpool = reinterpret_cast<uint16_t*>(a.kv_pool);
 #pragma unroll
       for (int i = 0; i < 8; ++i) vpool[vblk + static_cast<int64_t>(8 * c + i) * 16 + vcol] = vb[i];
     }
@@ -160,7 +162,7 @@ int launch_write(const WriteArgs& a, bool fp8, bool prefill, cudaStream_t s) {
 }
 
 int write_entry(bool fp8, bool prefill, const void* k, const void* v, const int32_t* seq_lens,
-                const int32_t* cu, int64_t rows, void* k_pool, void* v_pool, const float* k_scale,
+                const int32_t* cu, int64_t rows, void* kv_pool, const float* k_scale,
                 const float* v_scale, const int32_t* page_table, int32_t max_pages,
                 const uint32_t* live_tags, const uint32_t* expected_tags, uint8_t* abort_mask,
                 int32_t B, int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
@@ -169,17 +171,15 @@ int write_entry(bool fp8, bool prefill, const void* k, const void* v, const int3
   if (st != FPK_OK) return st;
   if (rows < 0) return FPK_EINVAL;
   if (rows == 0 || B == 0) return FPK_OK;
-  if (!k || !v || !k_pool || !v_pool || !page_table || (prefill ? !cu : !seq_lens))
-    return FPK_EINVAL;
+  if (!k || !v || !kv_pool || !page_table || (prefill ? !cu : !seq_lens)) return FPK_EINVAL;
   if (fp8 && (!k_scale || !v_scale)) return FPK_EINVAL;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool)) return FPK_EINVAL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kv_pool)) return FPK_EINVAL;
   WriteArgs a;
   a.k_src = static_cast<const uint16_t*>(k);
   a.v_src = static_cast<const uint16_t*>(v);
   a.seq_lens = seq_lens;
   a.cu_seqlens = cu;
-  a.k_pool = static_cast<uint8_t*>(k_pool);
-  a.v_pool = static_cast<uint8_t*>(v_pool);
+  a.kv_pool = static_cast<uint8_t*>(kv_pool);
   a.k_scale = k_scale;
   a.v_scale = v_scale;
   a.page_table = page_table;
@@ -199,48 +199,48 @@ int write_entry(bool fp8, bool prefill, const void* k, const void* v, const int3
 }  // namespace
 }  // namespace fpk
 
-extern "C" int fpk_kv_append_fp8(const void* k_new, const void* v_new, uint8_t* k_pool,
-                                 uint8_t* v_pool, const float* k_scale, const float* v_scale,
+extern "C" int fpk_kv_append_fp8(const void* k_new, const void* v_new, uint8_t* kv_pool,
+                                 const float* k_scale, const float* v_scale,
                                  const int32_t* page_table, int32_t max_pages,
                                  const int32_t* seq_lens, const uint32_t* live_tags,
                                  const uint32_t* expected_tags, uint8_t* abort_mask, int32_t B,
                                  int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
                                  void* stream) {
-  return fpk::write_entry(true, false, k_new, v_new, seq_lens, nullptr, B, k_pool, v_pool, k_scale,
+  return fpk::write_entry(true, false, k_new, v_new, seq_lens, nullptr, B, kv_pool, k_scale,
                           v_scale, page_table, max_pages, live_tags, expected_tags, abort_mask, B,
                           Hkv, D, page_size, num_pages, stream);
 }
 
-extern "C" int fpk_kv_append_bf16(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+extern "C" int fpk_kv_append_bf16(const void* k_new, const void* v_new, void* kv_pool,
                                   const int32_t* page_table, int32_t max_pages,
                                   const int32_t* seq_lens, const uint32_t* live_tags,
                                   const uint32_t* expected_tags, uint8_t* abort_mask, int32_t B,
                                   int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
                                   void* stream) {
-  return fpk::write_entry(false, false, k_new, v_new, seq_lens, nullptr, B, k_pool, v_pool, nullptr,
+  return fpk::write_entry(false, false, k_new, v_new, seq_lens, nullptr, B, kv_pool, nullptr,
                           nullptr, page_table, max_pages, live_tags, expected_tags, abort_mask, B,
                           Hkv, D, page_size, num_pages, stream);
 }
 
 extern "C" int fpk_kv_prefill_fp8(const void* k, const void* v, const int32_t* cu_seqlens,
-                                  int32_t n_tokens, uint8_t* k_pool, uint8_t* v_pool,
+                                  int32_t n_tokens, uint8_t* kv_pool,
                                   const float* k_scale, const float* v_scale,
                                   const int32_t* page_table, int32_t max_pages,
                                   const uint32_t* live_tags, const uint32_t* expected_tags,
                                   uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
                                   int32_t page_size, int32_t num_pages, void* stream) {
-  return fpk::write_entry(true, true, k, v, nullptr, cu_seqlens, n_tokens, k_pool, v_pool, k_scale,
+  return fpk::write_entry(true, true, k, v, nullptr, cu_seqlens, n_tokens, kv_pool, k_scale,
                           v_scale, page_table, max_pages, live_tags, expected_tags, abort_mask, B,
                           Hkv, D, page_size, num_pages, stream);
 }
 
 extern "C" int fpk_kv_prefill_bf16(const void* k, const void* v, const int32_t* cu_seqlens,
-                                   int32_t n_tokens, void* k_pool, void* v_pool,
+                                   int32_t n_tokens, void* kv_pool,
                                    const int32_t* page_table, int32_t max_pages,
                                    const uint32_t* live_tags, const uint32_t* expected_tags,
                                    uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
                                    int32_t page_size, int32_t num_pages, void* stream) {
-  return fpk::write_entry(false, true, k, v, nullptr, cu_seqlens, n_tokens, k_pool, v_pool, nullptr,
+  return fpk::write_entry(false, true, k, v, nullptr, cu_seqlens, n_tokens, kv_pool, nullptr,
                           nullptr, page_table, max_pages, live_tags, expected_tags, abort_mask, B,
                           Hkv, D, page_size, num_pages, stream);
 }

@@ -1,6 +1,6 @@
 """Device-resident decode pool: torch allocates, libfp8kv computes.
 
-A DecodePool holds one layer's paged KV cache (e4m3 or bf16), the page table,
+A DecodePool holds one layer's paged KV pool (e4m3 or bf16), the page table,
 the live and expected page tags, the per-tensor scales and the output and
 workspace buffers of a decode batch, and runs the decode step in the order
 the pages describe: write the new token's K/V into its page, check every
@@ -38,13 +38,11 @@ class DecodePool:
         self.fp8 = fp8
         self.device = torch.device(device)
         dev = self.device
-        n = wl.num_pages * wl.Hkv * wl.page_size * wl.D
+        n = 2 * wl.num_pages * wl.Hkv * wl.page_size * wl.D      # K and V of every slot
         if fp8:
-            self.k_pool = torch.full((n,), NAN_E4M3, dtype=torch.uint8, device=dev)
-            self.v_pool = torch.full((n,), NAN_E4M3, dtype=torch.uint8, device=dev)
+            self.kv_pool = torch.full((n,), NAN_E4M3, dtype=torch.uint8, device=dev)
         else:
-            self.k_pool = torch.full((n,), NAN_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
-            self.v_pool = torch.full((n,), NAN_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+            self.kv_pool = torch.full((n,), NAN_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
         self.page_table = to_device(wl.page_table, dev)
         self.live_tags = to_device(wl.live_tags, dev)
         self.expected_tags = to_device(wl.expected_tags, dev)
@@ -85,10 +83,10 @@ class DecodePool:
             pt = self.page_table[r0:r1]
             ex = self.expected_tags[r0:r1]
             if self.fp8:
-                fpk_kv_prefill_fp8(k, v, cu_sub, self.k_pool, self.v_pool, self.k_scale, self.v_scale,
+                fpk_kv_prefill_fp8(k, v, cu_sub, self.kv_pool, self.k_scale, self.v_scale,
                                    pt, self.live_tags, ex, None, **self.kw)
             else:
-                fpk_kv_prefill_bf16(k, v, cu_sub, self.k_pool, self.v_pool, pt, self.live_tags, ex,
+                fpk_kv_prefill_bf16(k, v, cu_sub, self.kv_pool, pt, self.live_tags, ex,
                                     None, **self.kw)
             del k, v
             r0 = r1
@@ -105,11 +103,11 @@ class DecodePool:
     def append(self, stream=None, guard: bool = True):
         tags = (self.live_tags, self.expected_tags, self.abort_mask) if guard else (None, None, None)
         if self.fp8:
-            fpk_kv_append_fp8(self.k_new, self.v_new, self.k_pool, self.v_pool, self.k_scale,
+            fpk_kv_append_fp8(self.k_new, self.v_new, self.kv_pool, self.k_scale,
                               self.v_scale, self.page_table, self.seq_lens, *tags, stream=stream,
                               **self.kw)
         else:
-            fpk_kv_append_bf16(self.k_new, self.v_new, self.k_pool, self.v_pool, self.page_table,
+            fpk_kv_append_bf16(self.k_new, self.v_new, self.kv_pool, self.page_table,
                                self.seq_lens, *tags, stream=stream, **self.kw)
 
     # ----------------------------------------------------------------- tags
@@ -129,11 +127,11 @@ class DecodePool:
         kw = dict(Hkv=wl.Hkv, page_size=wl.page_size, num_pages=wl.num_pages,
                   sm_scale=wl.sm_scale, num_splits=ns, stream=stream)
         if self.fp8:
-            fpk_paged_decode_attn_fp8(self.q, self.k_pool, self.v_pool, self.k_scale, self.v_scale,
+            fpk_paged_decode_attn_fp8(self.q, self.kv_pool, self.k_scale, self.v_scale,
                                       self.page_table, self.seq_lens, mask, self.out, self.lse,
                                       self.workspace, **kw)
         else:
-            fpk_paged_decode_attn_bf16(self.q, self.k_pool, self.v_pool, self.page_table,
+            fpk_paged_decode_attn_bf16(self.q, self.kv_pool, self.page_table,
                                        self.seq_lens, mask, self.out, self.lse, self.workspace, **kw)
 
     def step(self, validate: bool = True, stream=None):
@@ -147,8 +145,7 @@ class DecodePool:
 
     # ------------------------------------------------------------- readback
     def pool_bytes(self):
-        """Host copies of the pools as raw uint8 / uint16 numpy arrays."""
+        """Host copy of the KV pool as raw uint8 (e4m3) / uint16 (bf16) elements."""
         if self.fp8:
-            return self.k_pool.cpu().numpy(), self.v_pool.cpu().numpy()
-        return (self.k_pool.view(torch.int16).cpu().numpy().view(np.uint16),
-                self.v_pool.view(torch.int16).cpu().numpy().view(np.uint16))
+            return self.kv_pool.cpu().numpy()
+        return self.kv_pool.view(torch.int16).cpu().numpy().view(np.uint16)

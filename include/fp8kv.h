@@ -38,12 +38,17 @@
  * Supported sizes: D == 128; page_size a multiple of 16 in [16, 256];
  * 1 <= G <= 8; B, Hkv >= 1.  Others return FPK_EUNSUPPORTED.
  *
- * Pool layout (bytes per element: 1 for the e4m3 pool, 2 for the bf16 pool):
- *   K pool  [num_pages][Hkv][page_size][D]           token-major rows
- *   V pool  [num_pages][Hkv][page_size/16][D][16]     16-token column blocks,
- *                                                     dim-major inside a block
+ * KV pool layout (one pool per layer holding K and V; bytes per element: 1
+ * for the e4m3 pool, 2 for the bf16 pool):
+ *   kv_pool [num_pages][Hkv][page_size/16][2][16*D]
+ *   i.e. every page holds, per kv head, page_size/16 tiles of 16 tokens, and
+ *   each tile is its K block [16 tokens][D] (token-major) immediately
+ *   followed by its V block [D][16 tokens] (dim-major).  A tile's K and V are
+ *   therefore one contiguous 2*16*D-element run.
  *   Token t of a request lives in page page_table[r][t / page_size] at slot
- *   t % page_size.  Pool base pointers must be 16-byte aligned.
+ *   s = t % page_size: K element d at tile (s/16), row s%16, column d; V
+ *   element d at tile (s/16), row d, column s%16.  The pool pointer must be
+ *   16-byte aligned.
  * Page table:     int32  [B][max_pages]   (row-major; entries past a request's
  *                                          ceil(L/page_size) pages are ignored)
  * Expected tags:  uint32 [B][max_pages]   (same shape as the page table)
@@ -96,10 +101,10 @@ const char* fpk_status_str(int status);
  * of the shared cache).
  *
  * For every request r with L = seq_lens[r] >= 1 (seq_lens already counts the
- * new token) and every kv head h and dim d, writes
- *   k_pool[page][h][pos % page_size][d] = e4m3(float(k_new[r][h][d]) / *k_scale)
- * and the V value into its column block, pos = L - 1,
- * page = page_table[r][pos / page_size].
+ * new token) and every kv head h and dim d, writes the K element of slot
+ * pos % page_size of page page_table[r][pos / page_size] (pos = L - 1) as
+ *   e4m3(float(k_new[r][h][d]) / *k_scale)
+ * and the V element likewise with *v_scale, at their places in kv_pool.
  * Guard (fail closed): when pos / page_size >= max_pages, the page id is
  * outside [0, num_pages), or live_tags and expected_tags are both given and
  * live_tags[page] != expected_tags[r][pos / page_size], nothing of request r
@@ -108,7 +113,7 @@ const char* fpk_status_str(int status);
  *   k_new, v_new : bf16 [B][Hkv][D] (device)
  *   live_tags, expected_tags, abort_mask : nullable (NULL = no tag guard)
  */
-int fpk_kv_append_fp8(const void* k_new, const void* v_new, uint8_t* k_pool, uint8_t* v_pool,
+int fpk_kv_append_fp8(const void* k_new, const void* v_new, uint8_t* kv_pool,
                       const float* k_scale, const float* v_scale,
                       const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
                       const uint32_t* live_tags, const uint32_t* expected_tags,
@@ -118,7 +123,7 @@ int fpk_kv_append_fp8(const void* k_new, const void* v_new, uint8_t* k_pool, uin
 /* Same as fpk_kv_append_fp8 for the BF16 comparison cache: the bf16 bit
  * patterns are copied unchanged (pools hold uint16 elements).  The pages keep
  * BF16 caches where compute dominates ("Cosa ha cambiato...", last paragraphs). */
-int fpk_kv_append_bf16(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+int fpk_kv_append_bf16(const void* k_new, const void* v_new, void* kv_pool,
                        const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
                        const uint32_t* live_tags, const uint32_t* expected_tags,
                        uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
@@ -133,7 +138,7 @@ int fpk_kv_append_bf16(const void* k_new, const void* v_new, void* k_pool, void*
  *                cu_seqlens[B] == n_tokens.
  */
 int fpk_kv_prefill_fp8(const void* k, const void* v, const int32_t* cu_seqlens, int32_t n_tokens,
-                       uint8_t* k_pool, uint8_t* v_pool, const float* k_scale, const float* v_scale,
+                       uint8_t* kv_pool, const float* k_scale, const float* v_scale,
                        const int32_t* page_table, int32_t max_pages,
                        const uint32_t* live_tags, const uint32_t* expected_tags,
                        uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
@@ -141,7 +146,7 @@ int fpk_kv_prefill_fp8(const void* k, const void* v, const int32_t* cu_seqlens, 
 
 /* BF16-cache variant of fpk_kv_prefill_fp8 (bit copy). */
 int fpk_kv_prefill_bf16(const void* k, const void* v, const int32_t* cu_seqlens, int32_t n_tokens,
-                        void* k_pool, void* v_pool, const int32_t* page_table, int32_t max_pages,
+                        void* kv_pool, const int32_t* page_table, int32_t max_pages,
                         const uint32_t* live_tags, const uint32_t* expected_tags,
                         uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
                         int32_t page_size, int32_t num_pages, void* stream);
@@ -222,7 +227,7 @@ size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  *               splits per (request, kv head).
  *   sm_scale  : softmax scale (1/sqrt(D) for standard attention).
  */
-int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* kv_pool,
                               const float* k_scale, const float* v_scale,
                               const int32_t* page_table, int32_t max_pages,
                               const int32_t* seq_lens, const uint8_t* abort_mask,
@@ -232,8 +237,8 @@ int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* k_pool, const uint8_
                               void* stream);
 
 /* BF16-cache variant of fpk_paged_decode_attn_fp8: same semantics with
- * k_pool / v_pool holding bf16 values (no scales). */
-int fpk_paged_decode_attn_bf16(const void* q, const void* k_pool, const void* v_pool,
+ * kv_pool holding bf16 values (no scales). */
+int fpk_paged_decode_attn_bf16(const void* q, const void* kv_pool,
                                const int32_t* page_table, int32_t max_pages,
                                const int32_t* seq_lens, const uint8_t* abort_mask,
                                float* out, float* lse, void* workspace, size_t workspace_bytes,
@@ -248,7 +253,7 @@ int fpk_paged_decode_attn_bf16(const void* q, const void* k_pool, const void* v_
  * operator hosts and plugin interfaces that hand an operator only its inputs
  * and outputs, processes held to a fixed device-memory budget, and
  * latency-critical loops that cannot afford cudaMalloc's implicit device
- * synchronisation.  The caller still passes q, the pools, tables, out and lse.
+ * synchronisation.  The caller still passes q, the pool, tables, out and lse.
  *
  * Scratch: a fixed 16 MiB array inside the library, which every GPU that
  * loads the library holds until the process exits.  A batch whose workspace
@@ -263,7 +268,7 @@ int fpk_paged_decode_attn_bf16(const void* q, const void* k_pool, const void* v_
  * other host threads) race on it and must be serialised by the caller.  The
  * kernel's status word is not reported by this entry point.
  */
-int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* kv_pool,
                                       const float* k_scale, const float* v_scale,
                                       const int32_t* page_table, int32_t max_pages,
                                       const int32_t* seq_lens, const uint8_t* abort_mask,

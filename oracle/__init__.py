@@ -61,14 +61,14 @@ def _load():
             lib.orc_quantize_bf16.restype = ctypes.c_uint8
             lib.orc_quantize_bf16.argtypes = [ctypes.c_uint16, _F]
             lib.orc_quantize_bf16_array.argtypes = [_P, _I64, _F, _P]
-            lib.orc_kv_append.argtypes = [_P, _P, _I, _P, _P, _F, _F, _P, _I, _P,
+            lib.orc_kv_append.argtypes = [_P, _P, _I, _P, _F, _F, _P, _I, _P,
                                           _P, _P, _P, _I, _I, _I, _I, _I]
-            lib.orc_kv_prefill.argtypes = [_P, _P, _P, _I, _P, _P, _F, _F, _P, _I,
+            lib.orc_kv_prefill.argtypes = [_P, _P, _P, _I, _P, _F, _F, _P, _I,
                                            _P, _P, _P, _I, _I, _I, _I, _I]
             lib.orc_page_tags_bump.argtypes = [_P, _P, _I, _I]
             lib.orc_page_tags_validate.restype = _I
             lib.orc_page_tags_validate.argtypes = [_P, _P, _P, _I, _P, _I, _I, _I, _P]
-            lib.orc_paged_attention.argtypes = [_P, _P, _P, _I, _D, _D, _P, _I, _P, _P, _D,
+            lib.orc_paged_attention.argtypes = [_P, _P, _I, _D, _D, _P, _I, _P, _P, _D,
                                                 _I, _I, _I, _I, _I, _I, _P, _P, _P]
             lib.orc_dense_attention.argtypes = [_P, _P, _P, _I, _I, _D, _P, _P, _P]
             _lib = lib
@@ -118,26 +118,26 @@ def quantize_bf16(xbits, scale: float) -> np.ndarray:
 # cache writes, tags
 # --------------------------------------------------------------------------
 
-def kv_append(k_new, v_new, k_pool, v_pool, k_scale, v_scale, page_table, seq_lens,
+def kv_append(k_new, v_new, kv_pool, k_scale, v_scale, page_table, seq_lens,
               live_tags=None, expected_tags=None, abort_mask=None, *, fp8: bool,
               Hkv: int, D: int, page_size: int, num_pages: int):
     """One decode-step append per request at position seq_lens[r]-1 (in place)."""
     B, max_pages = page_table.shape
     _load().orc_kv_append(_ptr(_c(k_new, np.uint16)), _ptr(_c(v_new, np.uint16)), int(fp8),
-                          _ptr(k_pool), _ptr(v_pool), float(k_scale), float(v_scale),
+                          _ptr(kv_pool), float(k_scale), float(v_scale),
                           _ptr(_c(page_table, np.int32)), max_pages, _ptr(_c(seq_lens, np.int32)),
                           _ptr(live_tags), _ptr(expected_tags), _ptr(abort_mask),
                           B, Hkv, D, page_size, num_pages)
 
 
-def kv_prefill(k, v, cu_seqlens, k_pool, v_pool, k_scale, v_scale, page_table,
+def kv_prefill(k, v, cu_seqlens, kv_pool, k_scale, v_scale, page_table,
                live_tags=None, expected_tags=None, abort_mask=None, *, fp8: bool,
                Hkv: int, D: int, page_size: int, num_pages: int):
     """Write whole prompts: rows cu[r]..cu[r+1]-1 go to positions 0.. of request r."""
     B, max_pages = page_table.shape
     _load().orc_kv_prefill(_ptr(_c(k, np.uint16)), _ptr(_c(v, np.uint16)),
                            _ptr(_c(cu_seqlens, np.int32)), int(fp8),
-                           _ptr(k_pool), _ptr(v_pool), float(k_scale), float(v_scale),
+                           _ptr(kv_pool), float(k_scale), float(v_scale),
                            _ptr(_c(page_table, np.int32)), max_pages,
                            _ptr(live_tags), _ptr(expected_tags), _ptr(abort_mask),
                            B, Hkv, D, page_size, num_pages)
@@ -166,7 +166,7 @@ def page_tags_validate(page_table, expected_tags, seq_lens, live_tags, num_pages
 # attention
 # --------------------------------------------------------------------------
 
-def paged_attention(q, k_pool, v_pool, page_table, seq_lens, *, fp8: bool, k_scale=1.0,
+def paged_attention(q, kv_pool, page_table, seq_lens, *, fp8: bool, k_scale=1.0,
                     v_scale=1.0, abort_mask=None, sm_scale: float, Hkv: int, page_size: int,
                     num_pages: int):
     """fp64 decode attention over the page table; returns (out [B][Hq][D], lse [B][Hq])."""
@@ -178,7 +178,7 @@ def paged_attention(q, k_pool, v_pool, page_table, seq_lens, *, fp8: bool, k_sca
     lse = np.empty((B, Hq), np.float64)
     scores = np.empty(max(1, max_pages * page_size), np.float64)
     am = None if abort_mask is None else _c(abort_mask, np.uint8)
-    _load().orc_paged_attention(_ptr(qb), _ptr(k_pool), _ptr(v_pool), int(fp8),
+    _load().orc_paged_attention(_ptr(qb), _ptr(kv_pool), int(fp8),
                                 float(k_scale), float(v_scale), _ptr(pt), max_pages,
                                 _ptr(_c(seq_lens, np.int32)), _ptr(am), float(sm_scale),
                                 B, Hq, Hkv, D, page_size, num_pages,

@@ -42,11 +42,11 @@
  *   checked; an aborted or empty request yields out = 0, lse = -inf.
  *
  * Pool layout (the library's documented storage format, restated here from
- * its definition, not shared with it):
- *   K pool: [num_pages][Hkv][page_size][D]                  (token-major)
- *   V pool: [num_pages][Hkv][page_size/16][D][16]            (16-token column
- *           blocks, each block dim-major)
- *   element = 1 byte (e4m3 code) or 2 bytes (bf16 bit pattern).
+ * its definition, not shared with it): one KV pool per layer,
+ *   kv_pool[num_pages][Hkv][page_size/16][2][16*D]
+ * i.e. for every page, kv head and 16-token tile of the page, the tile's K
+ * block [16 tokens][D] (token-major) followed by its V block [D][16 tokens]
+ * (dim-major); element = 1 byte (e4m3 code) or 2 bytes (bf16 bit pattern).
  *
  * All floating point is fp64 except the single fp32 division x/scale that the
  * quantiser is defined on.  Build with -ffp-contract=off.
@@ -158,15 +158,20 @@ void orc_quantize_bf16_array(const uint16_t *xbits, int64_t n, float scale, uint
 /* pool indexing (the documented layout)                                      */
 /* ------------------------------------------------------------------------- */
 
+/* first element of the (K, V) block pair of the tile holding slot `off` */
+static int64_t tile_base(int64_t page, int h, int off, int Hkv, int ps, int D)
+{
+    return (((page * Hkv + h) * (int64_t)(ps / 16) + off / 16) * 2) * 16 * (int64_t)D;
+}
+
 static int64_t k_index(int64_t page, int h, int off, int d, int Hkv, int ps, int D)
 {
-    return ((page * Hkv + h) * (int64_t)ps + off) * D + d;
+    return tile_base(page, h, off, Hkv, ps, D) + (int64_t)(off % 16) * D + d;
 }
 
 static int64_t v_index(int64_t page, int h, int off, int d, int Hkv, int ps, int D)
 {
-    int blk = off / 16, col = off % 16;
-    return (((page * Hkv + h) * (int64_t)(ps / 16) + blk) * D + d) * 16 + col;
+    return tile_base(page, h, off, Hkv, ps, D) + 16 * (int64_t)D + (int64_t)d * 16 + off % 16;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -180,7 +185,7 @@ static int64_t v_index(int64_t page, int h, int off, int d, int Hkv, int ps, int
  * request in abort_mask (when given).  Returns 1 if written, 0 if skipped.
  */
 static int write_token(const uint16_t *krow, const uint16_t *vrow, int is_fp8,
-                       void *k_pool, void *v_pool, float k_scale, float v_scale,
+                       void *kv_pool, float k_scale, float v_scale,
                        const int32_t *page_table, int max_pages, int r, int pos,
                        const uint32_t *live_tags, const uint32_t *expected_tags,
                        uint8_t *abort_mask, int Hkv, int D, int ps, int num_pages)
@@ -207,11 +212,11 @@ static int write_token(const uint16_t *krow, const uint16_t *vrow, int is_fp8,
             int64_t ki = k_index(page, h, off, d, Hkv, ps, D);
             int64_t vi = v_index(page, h, off, d, Hkv, ps, D);
             if (is_fp8) {
-                ((uint8_t *)k_pool)[ki] = orc_quantize_bf16(kb, k_scale);
-                ((uint8_t *)v_pool)[vi] = orc_quantize_bf16(vb, v_scale);
+                ((uint8_t *)kv_pool)[ki] = orc_quantize_bf16(kb, k_scale);
+                ((uint8_t *)kv_pool)[vi] = orc_quantize_bf16(vb, v_scale);
             } else {
-                ((uint16_t *)k_pool)[ki] = kb;
-                ((uint16_t *)v_pool)[vi] = vb;
+                ((uint16_t *)kv_pool)[ki] = kb;
+                ((uint16_t *)kv_pool)[vi] = vb;
             }
         }
     }
@@ -224,7 +229,7 @@ static int write_token(const uint16_t *krow, const uint16_t *vrow, int is_fp8,
  * seq_lens[r] <= 0 append nothing.  k_new, v_new: bf16 [B][Hkv][D].
  */
 void orc_kv_append(const uint16_t *k_new, const uint16_t *v_new, int is_fp8,
-                   void *k_pool, void *v_pool, float k_scale, float v_scale,
+                   void *kv_pool, float k_scale, float v_scale,
                    const int32_t *page_table, int max_pages, const int32_t *seq_lens,
                    const uint32_t *live_tags, const uint32_t *expected_tags,
                    uint8_t *abort_mask, int B, int Hkv, int D, int ps, int num_pages)
@@ -235,7 +240,7 @@ void orc_kv_append(const uint16_t *k_new, const uint16_t *v_new, int is_fp8,
         if (L <= 0)
             continue;
         write_token(k_new + (int64_t)r * Hkv * D, v_new + (int64_t)r * Hkv * D, is_fp8,
-                    k_pool, v_pool, k_scale, v_scale, page_table, max_pages, r, L - 1,
+                    kv_pool, k_scale, v_scale, page_table, max_pages, r, L - 1,
                     live_tags, expected_tags, abort_mask, Hkv, D, ps, num_pages);
     }
 }
@@ -245,7 +250,7 @@ void orc_kv_append(const uint16_t *k_new, const uint16_t *v_new, int is_fp8,
  * k, v (bf16 [N][Hkv][D]) are request r's tokens at positions 0, 1, ...
  */
 void orc_kv_prefill(const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens, int is_fp8,
-                    void *k_pool, void *v_pool, float k_scale, float v_scale,
+                    void *kv_pool, float k_scale, float v_scale,
                     const int32_t *page_table, int max_pages,
                     const uint32_t *live_tags, const uint32_t *expected_tags,
                     uint8_t *abort_mask, int B, int Hkv, int D, int ps, int num_pages)
@@ -254,7 +259,7 @@ void orc_kv_prefill(const uint16_t *k, const uint16_t *v, const int32_t *cu_seql
     for (r = 0; r < B; ++r) {
         for (i = cu_seqlens[r]; i < cu_seqlens[r + 1]; ++i) {
             write_token(k + (int64_t)i * Hkv * D, v + (int64_t)i * Hkv * D, is_fp8,
-                        k_pool, v_pool, k_scale, v_scale, page_table, max_pages, r,
+                        kv_pool, k_scale, v_scale, page_table, max_pages, r,
                         i - cu_seqlens[r], live_tags, expected_tags, abort_mask,
                         Hkv, D, ps, num_pages);
         }
@@ -329,7 +334,7 @@ static double load_k(const void *pool, int is_fp8, int64_t idx, double scale)
  * Aborted (abort_mask[r] != 0), empty, over-long or out-of-range-page requests
  * give out = 0, lse = -inf.  scores: caller scratch of >= max_pages*ps doubles.
  */
-void orc_paged_attention(const uint16_t *q, const void *k_pool, const void *v_pool, int is_fp8,
+void orc_paged_attention(const uint16_t *q, const void *kv_pool, int is_fp8,
                          double k_scale, double v_scale, const int32_t *page_table, int max_pages,
                          const int32_t *seq_lens, const uint8_t *abort_mask, double sm_scale,
                          int B, int Hq, int Hkv, int D, int ps, int num_pages,
@@ -361,7 +366,7 @@ void orc_paged_attention(const uint16_t *q, const void *k_pool, const void *v_po
                 int64_t page = page_table[(int64_t)r * max_pages + j / ps];
                 double acc = 0.0;
                 for (d = 0; d < D; ++d) {
-                    double kv = load_k(k_pool, is_fp8, k_index(page, hk, j % ps, d, Hkv, ps, D), k_scale);
+                    double kv = load_k(kv_pool, is_fp8, k_index(page, hk, j % ps, d, Hkv, ps, D), k_scale);
                     acc += (double)bf16_bits_to_float(qr[d]) * kv;
                 }
                 scores[j] = acc * sm_scale;
@@ -373,7 +378,7 @@ void orc_paged_attention(const uint16_t *q, const void *k_pool, const void *v_po
                 double p = exp(scores[j] - m);
                 l += p;
                 for (d = 0; d < D; ++d)
-                    o[d] += p * load_k(v_pool, is_fp8, v_index(page, hk, j % ps, d, Hkv, ps, D), v_scale);
+                    o[d] += p * load_k(kv_pool, is_fp8, v_index(page, hk, j % ps, d, Hkv, ps, D), v_scale);
             }
             for (d = 0; d < D; ++d) o[d] /= l;
             lse[(int64_t)r * Hq + h] = m + log(l);

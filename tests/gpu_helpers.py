@@ -10,28 +10,27 @@ RTOL = 1e-2
 
 
 def oracle_pools(wl, fp8, fill=True):
-    """Oracle pools after the prompts are written (unwritten slots hold NaN codes)."""
+    """The oracle's KV pool after the prompts are written (unwritten slots hold NaN codes)."""
     dt = np.uint8 if fp8 else np.uint16
-    n = wl.num_pages * wl.Hkv * wl.page_size * wl.D
-    kp = np.full(n, 0x7F if fp8 else 0x7FC0, dt)
-    vp = np.full(n, 0x7F if fp8 else 0x7FC0, dt)
+    n = 2 * wl.num_pages * wl.Hkv * wl.page_size * wl.D
+    pool = np.full(n, 0x7F if fp8 else 0x7FC0, dt)
     if fill:
-        oracle.kv_prefill(wl.k_prompt, wl.v_prompt, wl.cu_prompt, kp, vp, wl.k_scale, wl.v_scale,
+        oracle.kv_prefill(wl.k_prompt, wl.v_prompt, wl.cu_prompt, pool, wl.k_scale, wl.v_scale,
                           wl.page_table, wl.live_tags, wl.expected_tags, None, fp8=fp8, Hkv=wl.Hkv,
                           D=wl.D, page_size=wl.page_size, num_pages=wl.num_pages)
-    return kp, vp
+    return pool
 
 
-def oracle_attention(wl, kp, vp, fp8, q, lens, abort=None, rows=None, page_table=None):
+def oracle_attention(wl, pool, fp8, q, lens, abort=None, rows=None, page_table=None):
     """fp64 oracle attention, optionally on a subset of requests (`rows`)."""
     pt = wl.page_table if page_table is None else page_table
     if rows is None:
-        return oracle.paged_attention(q, kp, vp, pt, lens, fp8=fp8, k_scale=wl.k_scale,
+        return oracle.paged_attention(q, pool, pt, lens, fp8=fp8, k_scale=wl.k_scale,
                                       v_scale=wl.v_scale, abort_mask=abort, sm_scale=wl.sm_scale,
                                       Hkv=wl.Hkv, page_size=wl.page_size, num_pages=wl.num_pages)
     rows = list(rows)
     sub_abort = None if abort is None else np.ascontiguousarray(abort[rows])
-    return oracle.paged_attention(np.ascontiguousarray(q[rows]), kp, vp, np.ascontiguousarray(pt[rows]),
+    return oracle.paged_attention(np.ascontiguousarray(q[rows]), pool, np.ascontiguousarray(pt[rows]),
                                   np.ascontiguousarray(lens[rows]), fp8=fp8, k_scale=wl.k_scale,
                                   v_scale=wl.v_scale, abort_mask=sub_abort, sm_scale=wl.sm_scale,
                                   Hkv=wl.Hkv, page_size=wl.page_size, num_pages=wl.num_pages)

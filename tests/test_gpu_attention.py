@@ -42,8 +42,8 @@ def _run_case(wl, fp8, num_splits, abort=None, use_mask=True, pt_override=None):
     pool.attend(use_mask=use_mask)
     torch.cuda.synchronize()
     assert pool.workspace[:4].view(torch.int32).item() == 0, "bounded wait gave up"
-    kp, vp = oracle_pools(wl, fp8)
-    ref_out, ref_lse = oracle_attention(wl, kp, vp, fp8, wl.q, lens,
+    ref = oracle_pools(wl, fp8)
+    ref_out, ref_lse = oracle_attention(wl, ref, fp8, wl.q, lens,
                                         abort=abort if use_mask else None, page_table=pt_override)
     return pool.out.cpu().numpy(), pool.lse.cpu().numpy(), ref_out, ref_lse
 
@@ -133,19 +133,18 @@ def test_tiny_full_step():
     pool.set_step(0)
     pool.step(validate=True)
     torch.cuda.synchronize()
-    kp, vp = oracle_pools(wl, True)
+    ref = oracle_pools(wl, True)
     kn, vn = wl.step_tokens(0)
     lens = wl.seq_lens_after(0)
     mask0 = np.zeros(2, np.uint8)
-    oracle.kv_append(kn, vn, kp, vp, wl.k_scale, wl.v_scale, wl.page_table, lens, wl.live_tags,
+    oracle.kv_append(kn, vn, ref, wl.k_scale, wl.v_scale, wl.page_table, lens, wl.live_tags,
                      wl.expected_tags, mask0, fp8=True, Hkv=wl.Hkv, D=wl.D, page_size=16,
                      num_pages=wl.num_pages)
-    gk, gv = pool.pool_bytes()
-    assert np.array_equal(gk, kp) and np.array_equal(gv, vp)
+    assert np.array_equal(pool.pool_bytes(), ref)
     mask, n = oracle.page_tags_validate(wl.page_table, wl.expected_tags, lens, wl.live_tags,
                                         wl.num_pages, 16)
     assert list(mask) == [0, 1] and np.array_equal(pool.abort_mask.cpu().numpy(), mask)
-    ro, rl = oracle_attention(wl, kp, vp, True, wl.q, lens, abort=mask)
+    ro, rl = oracle_attention(wl, ref, True, wl.q, lens, abort=mask)
     assert_attention_close(pool.out.cpu().numpy(), pool.lse.cpu().numpy(), ro, rl, "tiny")
 
 
@@ -166,13 +165,12 @@ def _sampled_full_size(wl, fp8, rows, steps=1, num_splits=None):
     assert pool.workspace[:4].view(torch.int32).item() == 0
     # oracle cache of the sampled requests only
     dt = np.uint8 if fp8 else np.uint16
-    npool = wl.num_pages * wl.Hkv * wl.page_size * wl.D
-    kp = np.full(npool, 0x7F if fp8 else 0x7FC0, dt)
-    vp = np.full(npool, 0x7F if fp8 else 0x7FC0, dt)
+    npool = 2 * wl.num_pages * wl.Hkv * wl.page_size * wl.D
+    ref = np.full(npool, 0x7F if fp8 else 0x7FC0, dt)
     for r in rows:
         a, b = int(wl.cu_prompt[r]), int(wl.cu_prompt[r + 1])
         cu = np.array([0, b - a], np.int32)
-        oracle.kv_prefill(wl.k_prompt[a:b], wl.v_prompt[a:b], cu, kp, vp, wl.k_scale, wl.v_scale,
+        oracle.kv_prefill(wl.k_prompt[a:b], wl.v_prompt[a:b], cu, ref, wl.k_scale, wl.v_scale,
                           wl.page_table[r:r + 1], wl.live_tags, wl.expected_tags[r:r + 1], None,
                           fp8=fp8, Hkv=wl.Hkv, D=wl.D, page_size=wl.page_size,
                           num_pages=wl.num_pages)
@@ -180,20 +178,20 @@ def _sampled_full_size(wl, fp8, rows, steps=1, num_splits=None):
         kn, vn = wl.step_tokens(s)
         lens = wl.seq_lens_after(s)
         for r in rows:
-            oracle.kv_append(kn[r:r + 1], vn[r:r + 1], kp, vp, wl.k_scale, wl.v_scale,
+            oracle.kv_append(kn[r:r + 1], vn[r:r + 1], ref, wl.k_scale, wl.v_scale,
                              wl.page_table[r:r + 1], lens[r:r + 1], wl.live_tags,
                              wl.expected_tags[r:r + 1], None, fp8=fp8, Hkv=wl.Hkv, D=wl.D,
                              page_size=wl.page_size, num_pages=wl.num_pages)
-    gk, gv = pool.pool_bytes()
+    got = pool.pool_bytes()
     for r in rows:
         P = -(-int(wl.seq_lens_after(steps - 1)[r]) // wl.page_size)
-        blk = wl.Hkv * wl.page_size * wl.D
+        blk = 2 * wl.Hkv * wl.page_size * wl.D          # one page: K and V of every kv head
         for page in wl.page_table[r, :P]:
             sl = slice(int(page) * blk, (int(page) + 1) * blk)
-            assert np.array_equal(gk[sl], kp[sl]) and np.array_equal(gv[sl], vp[sl]), (r, page)
+            assert np.array_equal(got[sl], ref[sl]), (r, page)
     lens = wl.seq_lens_after(steps - 1)
     q = wl.step_query(steps - 1)
-    ro, rl = oracle_attention(wl, kp, vp, fp8, q, lens, rows=rows)
+    ro, rl = oracle_attention(wl, ref, fp8, q, lens, rows=rows)
     out = pool.out.cpu().numpy()[rows]
     lse = pool.lse.cpu().numpy()[rows]
     return assert_attention_close(out, lse, ro, rl, f"{wl.name} fp8={fp8}")

@@ -69,19 +69,17 @@ def test_prefill_and_append_bytes_bit_exact(fp8, ps):
                 sigma=3.0, outlier_frac=0.05)
     pool = DecodePool(wl, fp8=fp8, device=DEV)
     pool.prefill()
-    kp, vp = oracle_pools(wl, fp8)
-    gk, gv = pool.pool_bytes()
-    assert np.array_equal(gk, kp) and np.array_equal(gv, vp)
+    ref = oracle_pools(wl, fp8)
+    assert np.array_equal(pool.pool_bytes(), ref)
     pool.set_step(0)
     pool.append()
     kn, vn = wl.step_tokens(0)
     lens = wl.seq_lens_after(0)
     mask = np.zeros(wl.B, np.uint8)
-    oracle.kv_append(kn, vn, kp, vp, wl.k_scale, wl.v_scale, wl.page_table, lens, wl.live_tags,
+    oracle.kv_append(kn, vn, ref, wl.k_scale, wl.v_scale, wl.page_table, lens, wl.live_tags,
                      wl.expected_tags, mask, fp8=fp8, Hkv=wl.Hkv, D=wl.D, page_size=ps,
                      num_pages=wl.num_pages)
-    gk, gv = pool.pool_bytes()
-    assert np.array_equal(gk, kp) and np.array_equal(gv, vp)
+    assert np.array_equal(pool.pool_bytes(), ref)
     assert np.array_equal(pool.abort_mask.cpu().numpy(), mask)
 
 
@@ -106,13 +104,12 @@ def test_guarded_append_bit_exact(what):
     pool.set_step(0)
     pool.seq_lens = to_device(lens, DEV)
     pool.append()
-    kp, vp = oracle_pools(wl, True, fill=False)
+    ref = oracle_pools(wl, True, fill=False)
     kn, vn = wl.step_tokens(0)
     mask = np.zeros(wl.B, np.uint8)
-    oracle.kv_append(kn, vn, kp, vp, wl.k_scale, wl.v_scale, pt, lens, wl.live_tags, ex, mask,
+    oracle.kv_append(kn, vn, ref, wl.k_scale, wl.v_scale, pt, lens, wl.live_tags, ex, mask,
                      fp8=True, Hkv=wl.Hkv, D=wl.D, page_size=ps, num_pages=wl.num_pages)
-    gk, gv = pool.pool_bytes()
-    assert np.array_equal(gk, kp) and np.array_equal(gv, vp)
+    assert np.array_equal(pool.pool_bytes(), ref)
     assert np.array_equal(pool.abort_mask.cpu().numpy(), mask)
     assert mask[r] == (0 if what == "none" else 1)
 

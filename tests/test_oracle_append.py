@@ -16,9 +16,11 @@ from workloads import bf16_bits, bf16_to_f32, custom
 
 
 def _slot_indices(page, h, off, Hkv, ps, D):
-    """Flat byte/element indices of one token's K row and V column (layout definition)."""
-    k = ((page * Hkv + h) * ps + off) * D + np.arange(D)
-    v = (((page * Hkv + h) * (ps // 16) + off // 16) * D + np.arange(D)) * 16 + off % 16
+    """Flat element indices of one token's K row and V column in the KV pool
+    [page][kv head][tile of 16 tokens][K block [16][D], V block [D][16]]."""
+    base = (((page * Hkv + h) * (ps // 16) + off // 16) * 2) * 16 * D
+    k = base + (off % 16) * D + np.arange(D)
+    v = base + 16 * D + np.arange(D) * 16 + off % 16
     return k, v
 
 
@@ -27,15 +29,14 @@ def _slot_indices(page, h, off, Hkv, ps, D):
 def test_append_writes_exactly_the_slot(fp8, ps):
     wl = custom(21, B=3, Hq=8, Hkv=2, ps=ps, prompt_lens=[5, ps, 2 * ps - 1])
     dt = np.uint8 if fp8 else np.uint16
-    n = wl.num_pages * wl.Hkv * ps * wl.D
+    n = 2 * wl.num_pages * wl.Hkv * ps * wl.D
     g = np.random.default_rng(1)
-    kp0 = g.integers(0, 256 if fp8 else 65536, size=n).astype(dt)
-    vp0 = g.integers(0, 256 if fp8 else 65536, size=n).astype(dt)
-    kp, vp = kp0.copy(), vp0.copy()
+    pool0 = g.integers(0, 256 if fp8 else 65536, size=n).astype(dt)
+    pool = pool0.copy()
     kn, vn = wl.step_tokens(0)
     lens = wl.seq_lens_after(0)
     mask = np.zeros(wl.B, np.uint8)
-    oracle.kv_append(kn, vn, kp, vp, wl.k_scale, wl.v_scale, wl.page_table, lens,
+    oracle.kv_append(kn, vn, pool, wl.k_scale, wl.v_scale, wl.page_table, lens,
                      wl.live_tags, wl.expected_tags, mask, fp8=fp8, Hkv=wl.Hkv, D=wl.D,
                      page_size=ps, num_pages=wl.num_pages)
     assert not mask.any()
@@ -52,25 +53,21 @@ def test_append_writes_exactly_the_slot(fp8, ps):
                 wantv = oracle.e4m3_encode(bf16_to_f32(vn[r, h]) / wl.v_scale)
             else:
                 wantk, wantv = kn[r, h], vn[r, h]
-            assert np.array_equal(kp[ki], wantk)
-            assert np.array_equal(vp[vi], wantv)
-    tk = np.concatenate(touched_k)
-    tv = np.concatenate(touched_v)
-    rest_k = np.ones(n, bool)
-    rest_k[tk] = False
-    rest_v = np.ones(n, bool)
-    rest_v[tv] = False
-    assert np.array_equal(kp[rest_k], kp0[rest_k])
-    assert np.array_equal(vp[rest_v], vp0[rest_v])
+            assert np.array_equal(pool[ki], wantk)
+            assert np.array_equal(pool[vi], wantv)
+    touched = np.concatenate(touched_k + touched_v)
+    assert np.unique(touched).size == touched.size      # K and V slots never overlap
+    rest = np.ones(n, bool)
+    rest[touched] = False
+    assert np.array_equal(pool[rest], pool0[rest])
 
 
 @pytest.mark.parametrize("what", ["stale", "page_oob", "neg_page", "beyond_table"])
 def test_guarded_append_skips_and_aborts(what):
     ps = 16
     wl = custom(22, B=2, Hq=4, Hkv=1, ps=ps, prompt_lens=[20, 40])
-    n = wl.num_pages * wl.Hkv * ps * wl.D
+    n = 2 * wl.num_pages * wl.Hkv * ps * wl.D
     kp = np.zeros(n, np.uint8)
-    vp = np.zeros(n, np.uint8)
     kn, vn = wl.step_tokens(0)
     lens = wl.seq_lens_after(0).copy()
     pt, exp = wl.page_table.copy(), wl.expected_tags.copy()
@@ -85,26 +82,26 @@ def test_guarded_append_skips_and_aborts(what):
     else:
         lens[r] = pt.shape[1] * ps + 1
     mask = np.zeros(2, np.uint8)
-    oracle.kv_append(kn, vn, kp, vp, wl.k_scale, wl.v_scale, pt, lens, wl.live_tags, exp, mask,
+    oracle.kv_append(kn, vn, kp, wl.k_scale, wl.v_scale, pt, lens, wl.live_tags, exp, mask,
                      fp8=True, Hkv=1, D=wl.D, page_size=ps, num_pages=wl.num_pages)
     assert list(mask) == [0, 1]
     # request 0 wrote its slot, request 1 wrote nothing
     page0 = int(pt[0, (int(lens[0]) - 1) // ps])
-    ki, _ = _slot_indices(page0, 0, (int(lens[0]) - 1) % ps, 1, ps, wl.D)
+    ki, vi = _slot_indices(page0, 0, (int(lens[0]) - 1) % ps, 1, ps, wl.D)
     written = np.zeros(n, bool)
     written[ki] = True
+    written[vi] = True
     assert not kp[~written].any()
 
 
 def test_no_tracker_means_no_tag_check():
     ps = 16
     wl = custom(23, B=1, Hq=4, Hkv=1, ps=ps, prompt_lens=[3])
-    n = wl.num_pages * ps * wl.D
+    n = 2 * wl.num_pages * ps * wl.D
     kp = np.zeros(n, np.uint8)
-    vp = np.zeros(n, np.uint8)
     kn, vn = wl.step_tokens(0)
     exp = wl.expected_tags + np.uint32(1)       # all stale, but no tags given below
-    oracle.kv_append(kn, vn, kp, vp, wl.k_scale, wl.v_scale, wl.page_table, wl.seq_lens_after(0),
+    oracle.kv_append(kn, vn, kp, wl.k_scale, wl.v_scale, wl.page_table, wl.seq_lens_after(0),
                      None, None, None, fp8=True, Hkv=1, D=wl.D, page_size=ps, num_pages=wl.num_pages)
     assert kp.any()
     del exp
@@ -115,10 +112,10 @@ def test_prefill_equals_token_by_token_append(fp8):
     ps = 16
     wl = custom(24, B=3, Hq=8, Hkv=2, ps=ps, prompt_lens=[1, 33, 16])
     dt = np.uint8 if fp8 else np.uint16
-    n = wl.num_pages * wl.Hkv * ps * wl.D
-    kp1, vp1 = np.zeros(n, dt), np.zeros(n, dt)
-    kp2, vp2 = np.zeros(n, dt), np.zeros(n, dt)
-    oracle.kv_prefill(wl.k_prompt, wl.v_prompt, wl.cu_prompt, kp1, vp1, wl.k_scale, wl.v_scale,
+    n = 2 * wl.num_pages * wl.Hkv * ps * wl.D
+    kp1 = np.zeros(n, dt)
+    kp2 = np.zeros(n, dt)
+    oracle.kv_prefill(wl.k_prompt, wl.v_prompt, wl.cu_prompt, kp1, wl.k_scale, wl.v_scale,
                       wl.page_table, wl.live_tags, wl.expected_tags, None, fp8=fp8, Hkv=wl.Hkv,
                       D=wl.D, page_size=ps, num_pages=wl.num_pages)
     maxlen = int(wl.prompt_lens.max())
@@ -131,10 +128,10 @@ def test_prefill_equals_token_by_token_append(fp8):
                 kn[r] = wl.k_prompt[wl.cu_prompt[r] + t]
                 vn[r] = wl.v_prompt[wl.cu_prompt[r] + t]
                 lens[r] = t + 1
-        oracle.kv_append(kn, vn, kp2, vp2, wl.k_scale, wl.v_scale, wl.page_table, lens,
+        oracle.kv_append(kn, vn, kp2, wl.k_scale, wl.v_scale, wl.page_table, lens,
                          wl.live_tags, wl.expected_tags, None, fp8=fp8, Hkv=wl.Hkv, D=wl.D,
                          page_size=ps, num_pages=wl.num_pages)
-    assert np.array_equal(kp1, kp2) and np.array_equal(vp1, vp2)
+    assert np.array_equal(kp1, kp2)
 
 
 def test_fp8_pool_is_half_the_bf16_bytes():

@@ -25,25 +25,28 @@ from workloads import bf16_bits, bf16_to_f32, custom
 
 
 def _pools(wl, fp8):
+    """The KV pool after the prompts are written (the oracle's own writer)."""
     dt = np.uint8 if fp8 else np.uint16
-    n = wl.num_pages * wl.Hkv * wl.page_size * wl.D
-    kp, vp = np.zeros(n, dt), np.zeros(n, dt)
-    oracle.kv_prefill(wl.k_prompt, wl.v_prompt, wl.cu_prompt, kp, vp, wl.k_scale, wl.v_scale,
+    n = 2 * wl.num_pages * wl.Hkv * wl.page_size * wl.D
+    pool = np.zeros(n, dt)
+    oracle.kv_prefill(wl.k_prompt, wl.v_prompt, wl.cu_prompt, pool, wl.k_scale, wl.v_scale,
                       wl.page_table, None, None, None, fp8=fp8, Hkv=wl.Hkv, D=wl.D,
                       page_size=wl.page_size, num_pages=wl.num_pages)
-    return kp, vp
+    return pool, pool
 
 
 def _gather(wl, kp, vp, fp8, r, h, L):
-    """Dense [L][D] float64 K-hat and V-hat of (request r, kv head h) from the pool layout."""
+    """Dense [L][D] float64 K-hat and V-hat of (request r, kv head h) from the pool layout
+    [page][kv head][tile of 16 tokens][K block [16][D], V block [D][16]]."""
     ps, D, Hkv = wl.page_size, wl.D, wl.Hkv
     K = np.empty((L, D))
     V = np.empty((L, D))
     for j in range(L):
         page = int(wl.page_table[r, j // ps])
         off = j % ps
-        ki = ((page * Hkv + h) * ps + off) * D + np.arange(D)
-        vi = (((page * Hkv + h) * (ps // 16) + off // 16) * D + np.arange(D)) * 16 + off % 16
+        base = (((page * Hkv + h) * (ps // 16) + off // 16) * 2) * 16 * D
+        ki = base + (off % 16) * D + np.arange(D)
+        vi = base + 16 * D + np.arange(D) * 16 + off % 16
         if fp8:
             K[j] = oracle.e4m3_decode(kp[ki]) * float(wl.k_scale)
             V[j] = oracle.e4m3_decode(vp[vi]) * float(wl.v_scale)
@@ -54,7 +57,8 @@ def _gather(wl, kp, vp, fp8, r, h, L):
 
 
 def _attn(wl, kp, vp, fp8, lens, abort=None, pt=None):
-    return oracle.paged_attention(wl.q, kp, vp, wl.page_table if pt is None else pt, lens, fp8=fp8,
+    assert kp is vp                                 # one KV pool
+    return oracle.paged_attention(wl.q, kp, wl.page_table if pt is None else pt, lens, fp8=fp8,
                                   k_scale=wl.k_scale, v_scale=wl.v_scale, abort_mask=abort,
                                   sm_scale=wl.sm_scale, Hkv=wl.Hkv, page_size=wl.page_size,
                                   num_pages=wl.num_pages)
@@ -131,12 +135,11 @@ def test_physical_page_permutation_invariance():
     out0, lse0 = _attn(wl, kp, vp, True, wl.prompt_lens)
     g = np.random.default_rng(3)
     perm = g.permutation(wl.num_pages)           # physical page p moves to perm[p]
-    blk = wl.Hkv * wl.page_size * wl.D
+    blk = 2 * wl.Hkv * wl.page_size * wl.D         # one page: K and V of every kv head
     kp2 = np.empty_like(kp)
-    vp2 = np.empty_like(vp)
     for p in range(wl.num_pages):
         kp2[perm[p] * blk:(perm[p] + 1) * blk] = kp[p * blk:(p + 1) * blk]
-        vp2[perm[p] * blk:(perm[p] + 1) * blk] = vp[p * blk:(p + 1) * blk]
+    vp2 = kp2
     pt2 = wl.page_table.copy()
     m = pt2 >= 0
     pt2[m] = perm[pt2[m]]
@@ -147,11 +150,11 @@ def test_physical_page_permutation_invariance():
 def test_power_of_two_k_scale_folds_into_query():
     wl = custom(36, B=1, Hq=4, Hkv=1, ps=16, prompt_lens=[45], steps=0)
     kp, vp = _pools(wl, True)
-    out_a, lse_a = oracle.paged_attention(wl.q, kp, vp, wl.page_table, wl.prompt_lens, fp8=True,
+    out_a, lse_a = oracle.paged_attention(wl.q, kp, wl.page_table, wl.prompt_lens, fp8=True,
                                           k_scale=4.0, v_scale=1.0, sm_scale=wl.sm_scale, Hkv=1,
                                           page_size=16, num_pages=wl.num_pages)
     q4 = bf16_bits(bf16_to_f32(wl.q) * np.float32(4))
-    out_b, lse_b = oracle.paged_attention(q4, kp, vp, wl.page_table, wl.prompt_lens, fp8=True,
+    out_b, lse_b = oracle.paged_attention(q4, kp, wl.page_table, wl.prompt_lens, fp8=True,
                                           k_scale=1.0, v_scale=1.0, sm_scale=wl.sm_scale, Hkv=1,
                                           page_size=16, num_pages=wl.num_pages)
     assert np.array_equal(out_a, out_b) and np.array_equal(lse_a, lse_b)
@@ -178,8 +181,11 @@ def test_gqa_head_mapping():
     out0, _ = _attn(wl, kp, vp, False, wl.prompt_lens)
     vp2 = vp.copy()
     page = int(wl.page_table[0, 0])
-    blk = wl.page_size * wl.D
-    vp2[(page * 2 + 1) * blk:(page * 2 + 2) * blk] = 0
-    out1, _ = _attn(wl, kp, vp2, False, wl.prompt_lens)
+    # zero kv head 1's V blocks on page 0 (each 16-token tile: K block, then V block)
+    D, ps = wl.D, wl.page_size
+    for t in range(ps // 16):
+        base = (((page * 2 + 1) * (ps // 16) + t) * 2) * 16 * D
+        vp2[base + 16 * D: base + 32 * D] = 0
+    out1, _ = _attn(wl, vp2, vp2, False, wl.prompt_lens)
     assert np.array_equal(out0[0, :4], out1[0, :4])
     assert not np.array_equal(out0[0, 4:], out1[0, 4:])

@@ -29,7 +29,7 @@ def _compare(pool, use_mask):
     ref_lse = pool.lse.clone()
     out = torch.full_like(pool.out, float("nan"))
     lse = torch.full_like(pool.lse, float("nan"))
-    fpk_paged_decode_attn_fp8_noalloc(pool.q, pool.k_pool, pool.v_pool, pool.k_scale, pool.v_scale,
+    fpk_paged_decode_attn_fp8_noalloc(pool.q, pool.kv_pool, pool.k_scale, pool.v_scale,
                                       pool.page_table, pool.seq_lens,
                                       pool.abort_mask if use_mask else None, out, lse, Hkv=wl.Hkv,
                                       page_size=wl.page_size, num_pages=wl.num_pages,
@@ -67,7 +67,7 @@ def test_noalloc_rejects_a_batch_larger_than_its_scratch():
     pool.prefill()
     with pytest.raises(FpkError, match="status 3"):
         # 20 000 splits need ~80 MB of partials, beyond the fixed 16 MiB
-        fpk_paged_decode_attn_fp8_noalloc(pool.q, pool.k_pool, pool.v_pool, pool.k_scale,
+        fpk_paged_decode_attn_fp8_noalloc(pool.q, pool.kv_pool, pool.k_scale,
                                           pool.v_scale, pool.page_table, pool.seq_lens, None,
                                           pool.out, pool.lse, Hkv=wl.Hkv, page_size=16,
                                           num_pages=wl.num_pages, sm_scale=wl.sm_scale,
