@@ -47,6 +47,7 @@ constexpr int kGroupMax = 8;     // query heads per kv head (N of the MMA tile)
 constexpr int kMergeStride = 132;  // floats per head row of the merge buffer
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
+static_assert(kConsumerWarps * 32 == 128, "the split-segment combine gives each consumer thread one of the 128 dims");
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -69,7 +70,7 @@ struct Cfg {
   // (m, l) per warp and head, then one fault flag per warp; rounded to 16 bytes
   // so that the mbarriers that follow stay 8-byte aligned for any warp count
   static constexpr int kMlBytes = (kConsumerWarps * kGroupMax * 4 * 2 + kConsumerWarps * 4 + 15) / 16 * 16;
-  static constexpr int kBarBytes = (2 * kStages + 2) * 8;
+  static constexpr int kBarBytes = (2 * kStages + 3) * 8;
   static constexpr int kSmemBytes = kRingBytes + kMergeBytes + kMlBytes + kBarBytes + kStages * 4 + 64;
 };
 
@@ -137,10 +138,7 @@ __device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, Piece& 
 __device__ __forceinline__ int worker_of(int64_t x, int64_t T, int W) {
   return static_cast<int>(((x + 1) * W - 1) / T);
 }
-// First worker after k that owns a tile: the owner of tile floor((k+1) T / W).
-__device__ __forceinline__ int next_worker(int k, int64_t T, int W) {
-  return worker_of(static_cast<int64_t>(k + 1) * T / W, T, W);
-}
+
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
@@ -166,11 +164,12 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   float* s_l = s_m + kConsumerWarps * kGroupMax;
   int* s_wfault = reinterpret_cast<int*>(s_l + kConsumerWarps * kGroupMax);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kMergeBytes + C::kMlBytes);
-  int* s_stage_fault = reinterpret_cast<int*>(bars + 2 * C::kStages + 2);
+  int* s_stage_fault = reinterpret_cast<int*>(bars + 2 * C::kStages + 3);
 
   __shared__ int64_t s_warp_sum[kThreads / 32];
   __shared__ int64_t s_total;
   __shared__ int s_start[4];
+  __shared__ int s_last;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -238,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   const uint32_t empty0 = full0 + 8 * C::kStages;
   const uint32_t merge_full = full0 + 16 * C::kStages;
   const uint32_t merge_free = merge_full + 8;
+  const uint32_t cbar = merge_free + 8;  // consumer-warp barrier of the split-segment combine
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     }
     mbar_init(merge_full, kConsumerWarps);
     mbar_init(merge_free, kConsumerWarps);
+    mbar_init(cbar, kConsumerWarps);
     fence_barrier_init();
   }
   __syncthreads();
@@ -375,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   Piece p;
   uint32_t jbase = 0;
   uint32_t piece_idx = 0;
+  uint32_t cphase = 0;  // completed phases of cbar
   bool ok = true;
   const float kNegInf = -INFINITY;
 
@@ -678,49 +680,72 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       }
     }
     if (!whole) {
-      // Arrival ticket per consumer warp: the warp that completes the count
-      // for this segment merges all its CTAs' partials (no waiting anywhere).
+      // Arrival ticket per CTA: the CTA that completes the count for this
+      // segment merges every contributing CTA's partial (nothing ever waits on
+      // another CTA).  All partial writes of this CTA are fenced first.
       __threadfence();
       __syncwarp();
-      const int64_t xseg = p.x0 - p.t0;  // global index of the segment's first tile
+      if (lane == 0) mbar_arrive(cbar);
+      bool got = mbar_wait(cbar, cphase & 1, a.status);
+      ++cphase;
+      if (!__all_sync(kFull, got)) break;
       const int64_t T = s_total;
+      const int64_t xseg = p.x0 - p.t0;  // global index of the segment's first tile
       const int w0 = worker_of(xseg, T, a.W);
       const int w1 = worker_of(xseg + p.n - 1, T, a.W);
       // CTAs holding a piece of this segment: all of w0..w1 when every worker
-      // owns tiles (T >= W), else one per tile
-      const int contributors = T >= a.W ? w1 - w0 + 1 : p.n;
-      int last = 0;
-      if (lane == 0) last = atomicAdd(a.seg_count + seg, 1) == contributors * kConsumerWarps - 1;
-      last = __shfl_sync(kFull, last, 0);
-      if (last) {
+      // owns tiles (T >= W), else one per tile (the i-th is the owner of tile i)
+      const bool dense = T >= a.W;
+      const int nsl = dense ? w1 - w0 + 1 : p.n;
+      if (ct == 0) {
+        s_last = atomicAdd(a.seg_count + seg, 1) == nsl - 1;
         __threadfence();
-        for (int hd = 0; hd < a.G; ++hd) {
-          float M = kNegInf;
-          bool dead = false;
-          for (int k = w0; k <= w1; k = next_worker(k, T, a.W)) {
-            const float2 ml = __ldcg(a.part_ml + (static_cast<int64_t>(seg) + k) * a.G + hd);
-            dead |= ml.y < 0.f;
-            M = fmaxf(M, ml.x);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cbar);
+      got = mbar_wait(cbar, cphase & 1, a.status);
+      ++cphase;
+      if (!__all_sync(kFull, got)) break;
+      if (s_last) {
+        __threadfence();
+        // one pass of online log-sum-exp over the contributing slots; thread ct
+        // owns dim d = ct of every head of the group
+        const int d = ct;
+        float M[kGroupMax], Wl[kGroupMax], acc[kGroupMax];
+        bool dead = false;
+#pragma unroll
+        for (int hd = 0; hd < kGroupMax; ++hd) M[hd] = kNegInf, Wl[hd] = 0.f, acc[hd] = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < nsl; ++i) {
+          const int k = dense ? w0 + i : worker_of(xseg + i, T, a.W);
+          const int64_t slot = static_cast<int64_t>(seg) + k;
+#pragma unroll
+          for (int hd = 0; hd < kGroupMax; ++hd) {
+            if (hd < a.G) {
+              const float2 ml = __ldcg(a.part_ml + slot * a.G + hd);
+              const float ov = __ldcg(a.part_o + (slot * a.G + hd) * kDim + d);
+              dead |= ml.y < 0.f;
+              if (ml.x != kNegInf) {
+                const float mn = fmaxf(M[hd], ml.x);
+                const float fo = M[hd] == kNegInf ? 0.f : fast_exp2(M[hd] - mn);
+                const float fk = fast_exp2(ml.x - mn);
+                Wl[hd] = Wl[hd] * fo + ml.y * fk;
+                acc[hd] = acc[hd] * fo + ov * fk;
+                M[hd] = mn;
+              }
+            }
           }
-          dead |= M == kNegInf;
-          float wsum = 0.f, acc[kDim / 32];
-#pragma unroll
-          for (int e = 0; e < kDim / 32; ++e) acc[e] = 0.f;
-          for (int k = w0; k <= w1 && !dead; k = next_worker(k, T, a.W)) {
-            const int64_t slot = static_cast<int64_t>(seg) + k;
-            const float2 ml = __ldcg(a.part_ml + slot * a.G + hd);
-            const float f = ml.x == kNegInf ? 0.f : fast_exp2(ml.x - M);
-            wsum += ml.y * f;
-            const float* po = a.part_o + (slot * a.G + hd) * kDim;
-#pragma unroll
-            for (int e = 0; e < kDim / 32; ++e) acc[e] += __ldcg(po + lane + 32 * e) * f;
-          }
-          const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
-#pragma unroll
-          for (int e = 0; e < kDim / 32; ++e) a.out[row * kDim + lane + 32 * e] = dead ? 0.f : acc[e] / wsum;
-          if (lane == 0 && a.lse != nullptr) a.lse[row] = dead ? kNegInf : (M + __log2f(wsum)) * kLn2;
         }
-        if (lane == 0) a.seg_count[seg] = 0;  // ready for the next call
+#pragma unroll
+        for (int hd = 0; hd < kGroupMax; ++hd) {
+          if (hd < a.G) {
+            const bool dh = dead || M[hd] == kNegInf;
+            const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
+            a.out[row * kDim + d] = dh ? 0.f : acc[hd] / Wl[hd];
+            if (d == 0 && a.lse != nullptr) a.lse[row] = dh ? kNegInf : (M[hd] + __log2f(Wl[hd])) * kLn2;
+          }
+        }
+        if (ct == 0) a.seg_count[seg] = 0;  // ready for the next call
       }
     }
     __syncwarp();
