@@ -147,14 +147,20 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def read_profile_traffic(workload: str):
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary."""
-    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
-    if os.path.exists(p):
-        with open(p) as f:
-            d = json.load(f)
-        return d.get("dram_bytes_per_launch")
-    return None
+def read_profile_traffic(workload: str, tag: str = "fp8"):
+    """Per-launch DRAM bytes (read + write) of the attention kernel from the committed
+    ncu record, or None when there is none or the kernel source changed since."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", f"paged_decode_attn_{tag}_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    csrc = os.path.join(ROOT, "fp8_paged_kv_gb300", "csrc")
+    src = b"".join(open(os.path.join(csrc, n), "rb").read() for n in ("decode_attn.cu", "common.cuh"))
+    if hashlib.sha256(src).hexdigest()[:16] != d.get("source_sha256_16"):
+        return None
+    return d.get("dram_bytes_per_launch")
 
 
 # ---------------------------------------------------------------------------
@@ -262,26 +268,69 @@ def time_steps(pool, steps: int, warmup: int, validate: bool = True):
     for _ in range(warmup):
         pool.step(validate=validate)
     torch.cuda.synchronize()
+    # the step as DecodePool.step runs it (write + tag check in one launch, then
+    # attention); events bracket each launch on the launching stream
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(s)
     for i in range(steps):
-        ev[i][0].record(s)
-        pool.append()
-        ev[i][1].record(s)
+        e = ev[i]
+        e[0].record(s)
         if validate:
-            pool.validate()
-        ev[i][2].record(s)
-        pool.attend(use_mask=validate)
-        ev[i][3].record(s)
+            pool.append_check(stream=s)
+        else:
+            pool.append(stream=s)
+        e[1].record(s)
+        e[2].record(s)
+        pool.attend(use_mask=validate, stream=s)
+        e[3].record(s)
     end.record(s)
     torch.cuda.synchronize()
     total_ms = start.elapsed_time(end)
     attn = [e[2].elapsed_time(e[3]) for e in ev]
-    val = [e[1].elapsed_time(e[2]) for e in ev]
     app = [e[0].elapsed_time(e[1]) for e in ev]
-    return total_ms, statistics.mean(attn), statistics.mean(val), statistics.mean(app)
+    return total_ms, statistics.mean(attn), statistics.mean(app)
+
+
+def capture_step(pool, validate: bool = True, io=None):
+    """One decode step (and, for io=(h2d, d2h) callables, its host copies) as a CUDA graph."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            if io:
+                io[0]()
+            pool.step(validate=validate)
+            if io:
+                io[1]()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        if io:
+            io[0]()
+        pool.step(validate=validate)
+        if io:
+            io[1]()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, steps: int, warmup: int) -> float:
+    """Device ms per replay of a captured step (events on the replay stream)."""
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(steps):
+        g.replay()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
 
 
 def time_e2e(pool, steps: int, warmup: int):
@@ -299,27 +348,20 @@ def time_e2e(pool, steps: int, warmup: int):
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_len))
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_mask))
 
-    def one():
+    def h2d_copies():
         pool.q.copy_(h_q, non_blocking=True)
         pool.k_new.copy_(h_k, non_blocking=True)
         pool.v_new.copy_(h_v, non_blocking=True)
         pool.seq_lens.copy_(h_len, non_blocking=True)
-        pool.step(validate=True)
+
+    def d2h_copies():
         h_out.copy_(pool.out, non_blocking=True)
         h_lse.copy_(pool.lse, non_blocking=True)
         h_mask.copy_(pool.abort_mask, non_blocking=True)
 
-    for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(s)
-    for _ in range(steps):
-        one()
-    b.record(s)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+    g = capture_step(pool, True, io=(h2d_copies, d2h_copies))
+    ms = time_graph(g, steps, warmup)
+    del s
     return ms, h2d, d2h
 
 
@@ -359,18 +401,24 @@ def main():
     torch.cuda.synchronize()
     live = int(wl.B - int(pool.abort_count.item()))
 
+    # the decode step as one CUDA graph (tag check next to the append, attention after both);
+    # the mismatch count is taken on the host from the abort mask the step returns
+    pool.count_aborts = False
+    g_step = capture_step(pool, True)
+    g_noval = capture_step(pool, False)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        total_ms, attn_ms, val_ms, app_ms = time_steps(pool, args.steps, args.warmup)
+        ms_step = time_graph(g_step, args.steps, args.warmup)
     barrier(world)
-    total_ms = max_over_ranks(total_ms, world)
-    ms_step = total_ms / args.steps
+    ms_step = max_over_ranks(ms_step, world)
     value = live * world / (ms_step * 1e-3)
 
-    # validation overhead: the same step with the no-op tracker
-    noval_ms, _, _, _ = time_steps(pool, max(args.steps // 4, 20), 3, validate=False)
-    noval_step = noval_ms / max(args.steps // 4, 20)
+    # per-kernel device times: the same step launched kernel by kernel, with events
+    # between the launches on their streams (the attention time is the roofline's)
+    _, attn_ms, app_ms = time_steps(pool, max(args.steps // 4, 20), 3)
+    # validation overhead: the same graph with the no-op tracker
+    noval_step = time_graph(g_noval, max(args.steps // 2, 20), 3)
     status = fpk.fpk_decode_status(pool.workspace)
 
     e2e_ms, h2d, d2h = time_e2e(pool, max(args.steps // 4, 20), 3)
@@ -386,20 +434,21 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache; f16 MMA, fp32 softmax",
         "data": "synthetic", "config": workload_config(wl),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": read_profile_traffic(wl.name),
+                     "frac": achieved / peak, "traffic": read_profile_traffic(wl.name, "fp8"),
                      "kernel": "paged_decode attention (split-KV, FP8)",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
-        "fp8": {"attn_us": attn_ms * 1e3, "validate_us": val_ms * 1e3, "append_us": app_ms * 1e3,
+        "fp8": {"attn_us": attn_ms * 1e3, "append_and_check_us": app_ms * 1e3,
                 "attn_tokens_per_s": live * world / (attn_ms * 1e-3),
-                "attn_gbs": achieved, "step_us_without_validation": noval_step * 1e3,
+                "attn_gbs": achieved, "step_us_without_validation": noval_step * 1e3, "step_launch": "CUDA graph per step",
                 "validation_overhead_pct": 100.0 * (ms_step - noval_step) / noval_step,
                 "algorithmic_bytes_per_attention": abytes, "status_word": status},
         "gpu_launches": None, "clocks": clk.summary(),
         "e2e": {"value": live * world / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
     }
-    launches_per_step = 3  # append, validate, attention (the combine is inside the attention kernel)
+    # per replayed step: append, validate, attention (the combine is inside the attention kernel)
+    launches_per_step = 3
     if args.steps:
         out["gpu_launches"] = launches_per_step * args.steps
     del pool
@@ -410,13 +459,17 @@ def main():
         p16 = DecodePool(wl, fp8=False, device=torch.device("cuda", torch.cuda.current_device()))
         p16.prefill()
         p16.set_step(0)
+        p16.count_aborts = False
         n16 = max(args.steps // 4, 20)
-        t16, a16, v16, _ = time_steps(p16, n16, args.warmup)
+        _, a16, _ = time_steps(p16, n16, args.warmup)
+        g16 = capture_step(p16, True)
+        t16 = time_graph(g16, n16, args.warmup) * n16
         b16 = attention_bytes(wl, 0, False)
         out["bf16"] = {"value": live * world / (t16 / n16 * 1e-3), "ms_per_step": t16 / n16,
                        "attn_us": a16 * 1e3, "attn_gbs": b16 / (a16 * 1e-3) / 1e9,
                        "attn_frac": b16 / (a16 * 1e-3) / 1e9 / peak,
-                       "fp8_over_bf16_step": (t16 / n16) / ms_step}
+                       "fp8_over_bf16_step": (t16 / n16) / ms_step,
+                       "traffic": read_profile_traffic(wl.name, "bf16")}
         del p16
         torch.cuda.empty_cache()
 

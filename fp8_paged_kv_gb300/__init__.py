@@ -45,6 +45,10 @@ SIGNATURES = {
     "fpk_quantize_e4m3": (ctypes.c_int, [_P, _P, _P, _I64, _P]),
     "fpk_page_tags_bump": (ctypes.c_int, [_P, _P, _I32, _I32, _P]),
     "fpk_page_tags_validate": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I32, _P, _P, _P]),
+    "fpk_decode_append_check_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P,
+                                                   _I32, _I32, _I32, _I32, _I32, _P]),
+    "fpk_decode_append_check_bf16": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P,
+                                                    _I32, _I32, _I32, _I32, _I32, _P]),
     "fpk_decode_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "fpk_paged_decode_attn_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
                                                  _SZ, _I32, _F, _I32, _I32, _I32, _I32, _I32, _I32,
@@ -174,6 +178,32 @@ def fpk_kv_prefill_bf16(k, v, cu_seqlens, kv_pool, page_table, live_tags=None,
         _ptr(live_tags, _TAGS, "live_tags", True), _ptr(expected_tags, _TAGS, "expected_tags", True),
         _ptr(abort_mask, _U8, "abort_mask", True), B, Hkv, D, page_size, num_pages,
         _stream(stream)), "fpk_kv_prefill_bf16")
+
+
+def fpk_decode_append_check_fp8(k_new, v_new, kv_pool, k_scale, v_scale, page_table, seq_lens,
+                                live_tags, expected_tags, abort_mask, *, Hkv, D, page_size,
+                                num_pages, stream=None):
+    B, max_pages = page_table.shape
+    _check(load_library().fpk_decode_append_check_fp8(
+        _ptr(k_new, _BF16_LIKE, "k_new"), _ptr(v_new, _BF16_LIKE, "v_new"),
+        _ptr(kv_pool, _U8, "kv_pool"), _ptr(k_scale, _F32, "k_scale"), _ptr(v_scale, _F32, "v_scale"),
+        _ptr(page_table, _I32T, "page_table"), max_pages, _ptr(seq_lens, _I32T, "seq_lens"),
+        _ptr(live_tags, _TAGS, "live_tags"), _ptr(expected_tags, _TAGS, "expected_tags"),
+        _ptr(abort_mask, _U8, "abort_mask"), B, Hkv, D, page_size, num_pages, _stream(stream)),
+        "fpk_decode_append_check_fp8")
+
+
+def fpk_decode_append_check_bf16(k_new, v_new, kv_pool, page_table, seq_lens, live_tags,
+                                 expected_tags, abort_mask, *, Hkv, D, page_size, num_pages,
+                                 stream=None):
+    B, max_pages = page_table.shape
+    _check(load_library().fpk_decode_append_check_bf16(
+        _ptr(k_new, _BF16_LIKE, "k_new"), _ptr(v_new, _BF16_LIKE, "v_new"),
+        _ptr(kv_pool, _BF16_LIKE, "kv_pool"),
+        _ptr(page_table, _I32T, "page_table"), max_pages, _ptr(seq_lens, _I32T, "seq_lens"),
+        _ptr(live_tags, _TAGS, "live_tags"), _ptr(expected_tags, _TAGS, "expected_tags"),
+        _ptr(abort_mask, _U8, "abort_mask"), B, Hkv, D, page_size, num_pages, _stream(stream)),
+        "fpk_decode_append_check_bf16")
 
 
 def fpk_quantize_e4m3(x, scale, out, stream=None):

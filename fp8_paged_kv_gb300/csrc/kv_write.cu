@@ -12,108 +12,19 @@
 // bf16 load per tensor, an 8-byte (fp8) or 16-byte (bf16) store into the
 // token-major K block of the token's 16-token tile, and 8 strided element
 // stores into the tile's dim-major V block.
-#include "common.cuh"
+#include "step_ops.cuh"
 
 namespace fpk {
 namespace {
 
-struct WriteArgs {
-  const uint16_t* k_src;     // bf16 [rows][Hkv][D]
-  const uint16_t* v_src;
-  const int32_t* seq_lens;   // decode mode: position = seq_lens[r] - 1, row r
-  const int32_t* cu_seqlens; // prefill mode: row i of request r at position i - cu[r]
-  uint8_t* kv_pool;
-  const float* k_scale;
-  const float* v_scale;
-  const int32_t* page_table;
-  const uint32_t* live_tags;
-  const uint32_t* expected_tags;
-  uint8_t* abort_mask;
-  int64_t rows;
-  int B, Hkv, D, page_size, num_pages, max_pages;
-};
-
-__device__ __forceinline__ int request_of_row(const int32_t* cu, int B, int64_t row) {
-  // largest r with cu[r] <= row (cu non-decreasing, cu[0] = 0)
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(__ldg(cu + mid)) <= row) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
 template <bool kFp8, bool kPrefill>
 __global__ void __launch_bounds__(256) write_tokens_kernel(WriteArgs a) {
-  const int chunks = a.D >> 3;
-  const int64_t units = a.rows * a.Hkv * chunks;
+  const int64_t units = a.rows * a.Hkv * (a.D >> 3);
   const float ks = kFp8 ? __ldg(a.k_scale) : 1.f;
   const float vs = kFp8 ? __ldg(a.v_scale) : 1.f;
   for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
-       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(u % chunks);
-    const int h = static_cast<int>((u / chunks) % a.Hkv);
-    const int64_t row = u / (static_cast<int64_t>(chunks) * a.Hkv);
-    int r, pos;
-    if (kPrefill) {
-      r = request_of_row(a.cu_seqlens, a.B, row);
-      pos = static_cast<int>(row - __ldg(a.cu_seqlens + r));
-    } else {
-      r = static_cast<int>(row);
-      pos = __ldg(a.seq_lens + r) - 1;
-      if (pos < 0) continue;
-    }
-    const int pi = pos / a.page_size;
-    const int off = pos - pi * a.page_size;
-    bool ok = pi < a.max_pages;
-    int page = -1;
-    if (ok) {
-      page = __ldg(a.page_table + static_cast<int64_t>(r) * a.max_pages + pi);
-      ok = page >= 0 && page < a.num_pages;
-    }
-    if (ok && a.live_tags != nullptr && a.expected_tags != nullptr)
-      ok = __ldg(a.live_tags + page) ==
-           __ldg(a.expected_tags + static_cast<int64_t>(r) * a.max_pages + pi);
-    if (!ok) {
-      if (a.abort_mask != nullptr) a.abort_mask[r] = 1;
-      continue;
-    }
-    const int64_t src = (row * a.Hkv + h) * a.D + 8 * c;
-    const uint4 kraw = __ldg(reinterpret_cast<const uint4*>(a.k_src + src));
-    const uint4 vraw = __ldg(reinterpret_cast<const uint4*>(a.v_src + src));
-    // the token's 16-token tile: K block [16][D], then V block [D][16]
-    const int64_t tile = ((static_cast<int64_t>(page) * a.Hkv + h) * (a.page_size >> 4) + (off >> 4)) *
-                         2 * 16 * a.D;
-    const int64_t kdst = tile + (off & 15) * a.D + 8 * c;
-    const int64_t vblk = tile + 16 * a.D;
-    const int vcol = off & 15;
-    const uint16_t* kb = reinterpret_cast<const uint16_t*>(&kraw);
-    const uint16_t* vb = reinterpret_cast<const uint16_t*>(&vraw);
-    if (kFp8) {
-      uint32_t kw[2];
-      uint8_t vq[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float k0 = __fdiv_rn(bf16_bits_to_float(kb[2 * i]), ks);
-        const float k1 = __fdiv_rn(bf16_bits_to_float(kb[2 * i + 1]), ks);
-        const float v0 = __fdiv_rn(bf16_bits_to_float(vb[2 * i]), vs);
-        const float v1 = __fdiv_rn(bf16_bits_to_float(vb[2 * i + 1]), vs);
-        const uint16_t kp = __nv_cvt_float2_to_fp8x2(make_float2(k0, k1), __NV_SATFINITE, __NV_E4M3);
-        const uint16_t vp = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
-        if (i & 1) kw[i >> 1] |= static_cast<uint32_t>(kp) << 16; else kw[i >> 1] = kp;
-        vq[2 * i] = static_cast<uint8_t>(vp & 0xFF);
-        vq[2 * i + 1] = static_cast<uint8_t>(vp >> 8);
-      }
-      *reinterpret_cast<uint2*>(a.kv_pool + kdst) = make_uint2(kw[0], kw[1]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a.kv_pool[vblk + static_cast<int64_t>(8 * c + i) * 16 + vcol] = vq[i];
-    } else {
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.kv_pool) + kdst) = kraw;
-      uint16_t* vpool = reinterpret_cast<uint16_t*>(a.kv_pool);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) vpool[vblk + static_cast<int64_t>(8 * c + i) * 16 + vcol] = vb[i];
-    }
-  }
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    write_unit<kFp8, kPrefill>(a, u, ks, vs);
 }
 
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ x,

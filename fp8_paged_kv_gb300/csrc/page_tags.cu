@@ -9,7 +9,7 @@
 // The check is its own batched kernel -- a pure gather-compare -- and is not
 // fused into attention (the same section: fusing it raced between GPU thread
 // groups).
-#include "common.cuh"
+#include "step_ops.cuh"
 
 namespace fpk {
 namespace {
@@ -23,43 +23,13 @@ __global__ void __launch_bounds__(256) bump_kernel(uint32_t* __restrict__ live_t
   if (p >= 0 && p < num_pages) atomicAdd(live_tags + p, 1u);
 }
 
-// One CTA per request.  Each thread checks up to 4 table entries per round
-// with all loads of the round issued before any compare.
-constexpr int kValidateThreads = 256;
-
 __global__ void __launch_bounds__(kValidateThreads) validate_kernel(
     const int32_t* __restrict__ page_table, const uint32_t* __restrict__ expected_tags,
     const int32_t* __restrict__ seq_lens, int max_pages, const uint32_t* __restrict__ live_tags,
     int num_pages, int page_size, uint8_t* __restrict__ abort_mask, int32_t* __restrict__ abort_count) {
-  const int r = blockIdx.x;
-  const int L = __ldg(seq_lens + r);
-  const int P = L > 0 ? (L + page_size - 1) / page_size : 0;
-  int bad = P > max_pages;
-  const int32_t* pt = page_table + static_cast<int64_t>(r) * max_pages;
-  const uint32_t* ex = expected_tags + static_cast<int64_t>(r) * max_pages;
-  for (int base = 0; base < P && !bad; base += 4 * kValidateThreads) {
-    int page[4];
-    uint32_t want[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = base + k * kValidateThreads + threadIdx.x;
-      page[k] = i < P ? __ldg(pt + i) : 0;
-      want[k] = i < P ? __ldg(ex + i) : 0u;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = base + k * kValidateThreads + threadIdx.x;
-      if (i < P) {
-        if (page[k] < 0 || page[k] >= num_pages) bad = 1;
-        else if (__ldg(live_tags + page[k]) != want[k]) bad = 1;
-      }
-    }
-  }
-  bad = __syncthreads_or(bad);
-  if (threadIdx.x == 0) {
-    abort_mask[r] = static_cast<uint8_t>(bad != 0);
-    if (bad && abort_count != nullptr) atomicAdd(abort_count, 1);
-  }
+  const int bad = check_request(page_table, expected_tags, seq_lens, max_pages, live_tags, num_pages,
+                                page_size, abort_mask, blockIdx.x);
+  if (threadIdx.x == 0 && bad && abort_count != nullptr) atomicAdd(abort_count, 1);
 }
 
 }  // namespace

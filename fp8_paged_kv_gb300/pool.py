@@ -14,7 +14,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (fpk_decode_workspace_bytes, fpk_kv_append_bf16, fpk_kv_append_fp8,
+from . import (fpk_decode_append_check_bf16, fpk_decode_append_check_fp8,
+               fpk_decode_workspace_bytes, fpk_kv_append_bf16, fpk_kv_append_fp8,
                fpk_kv_prefill_bf16, fpk_kv_prefill_fp8, fpk_page_tags_bump,
                fpk_page_tags_validate, fpk_paged_decode_attn_bf16, fpk_paged_decode_attn_fp8)
 
@@ -59,6 +60,7 @@ class DecodePool:
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
         self.k_new = None
         self.v_new = None
+        self.count_aborts = True
 
     @property
     def kw(self):
@@ -115,9 +117,12 @@ class DecodePool:
         fpk_page_tags_bump(self.live_tags, pages, num_pages=self.wl.num_pages, stream=stream)
 
     def validate(self, stream=None):
+        # count_aborts=False skips the device-side count (and its zeroing); the
+        # abort mask alone carries the same information to the host
         fpk_page_tags_validate(self.page_table, self.expected_tags, self.seq_lens, self.live_tags,
-                               self.abort_mask, self.abort_count, num_pages=self.wl.num_pages,
-                               page_size=self.wl.page_size, stream=stream)
+                               self.abort_mask, self.abort_count if self.count_aborts else None,
+                               num_pages=self.wl.num_pages, page_size=self.wl.page_size,
+                               stream=stream)
 
     # ------------------------------------------------------------ attention
     def attend(self, use_mask: bool = True, stream=None, num_splits: int | None = None):
@@ -134,14 +139,35 @@ class DecodePool:
             fpk_paged_decode_attn_bf16(self.q, self.kv_pool, self.page_table,
                                        self.seq_lens, mask, self.out, self.lse, self.workspace, **kw)
 
-    def step(self, validate: bool = True, stream=None):
-        """One decode step: append, (validate), attend."""
-        self.append(stream=stream)
-        if validate:
-            self.validate(stream=stream)
-            self.attend(use_mask=True, stream=stream)
+    def append_check(self, stream=None):
+        """The step's cache write and batched tag check in one launch."""
+        if self.fp8:
+            fpk_decode_append_check_fp8(self.k_new, self.v_new, self.kv_pool, self.k_scale,
+                                        self.v_scale, self.page_table, self.seq_lens,
+                                        self.live_tags, self.expected_tags, self.abort_mask,
+                                        stream=stream, **self.kw)
         else:
-            self.attend(use_mask=False, stream=stream)
+            fpk_decode_append_check_bf16(self.k_new, self.v_new, self.kv_pool, self.page_table,
+                                         self.seq_lens, self.live_tags, self.expected_tags,
+                                         self.abort_mask, stream=stream, **self.kw)
+
+    def step(self, validate: bool = True, stream=None):
+        """One decode step.  With validation: the cache write and the batched tag
+        check (one launch; a separate operation from attention), then attention
+        over the requests that passed.  Without it (the no-op tracker): the
+        write, then attention with no tag check.  With count_aborts the check
+        runs as its own launch so that it also produces the device-side count."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if not validate:
+            self.append(stream=main)
+            self.attend(use_mask=False, stream=main)
+            return
+        if self.count_aborts:
+            self.append(stream=main)
+            self.validate(stream=main)
+        else:
+            self.append_check(stream=main)
+        self.attend(use_mask=True, stream=main)
 
     # ------------------------------------------------------------- readback
     def pool_bytes(self):

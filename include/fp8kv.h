@@ -187,6 +187,31 @@ int fpk_page_tags_validate(const int32_t* page_table, const uint32_t* expected_t
                            void* stream);
 
 /*
+ * One launch carrying a decode step's cache write and its batched tag check:
+ * exactly fpk_kv_append_fp8 (with the tag guard) followed by
+ * fpk_page_tags_validate (without abort_count), for the same arguments.  The
+ * check remains a separate batched operation, kept out of attention ("La
+ * sicurezza della cache KV condivisa..."); sharing a launch with the write is
+ * safe because the two touch disjoint data, and wherever the write refuses a
+ * stale slot the check marks the same request for the same table entry.
+ * abort_mask (uint8 [B]) is overwritten with the check's result; live_tags and
+ * expected_tags are required.
+ */
+int fpk_decode_append_check_fp8(const void* k_new, const void* v_new, uint8_t* kv_pool,
+                                const float* k_scale, const float* v_scale,
+                                const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                                const uint32_t* live_tags, const uint32_t* expected_tags,
+                                uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
+                                int32_t page_size, int32_t num_pages, void* stream);
+
+/* BF16-cache variant of fpk_decode_append_check_fp8 (bit copy, no scales). */
+int fpk_decode_append_check_bf16(const void* k_new, const void* v_new, void* kv_pool,
+                                 const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                                 const uint32_t* live_tags, const uint32_t* expected_tags,
+                                 uint8_t* abort_mask, int32_t B, int32_t Hkv, int32_t D,
+                                 int32_t page_size, int32_t num_pages, void* stream);
+
+/*
  * Workspace (device bytes) that fpk_paged_decode_attn_* needs for this batch
  * shape and split count.  num_splits == 0 means the automatic count the
  * attention call would choose on the CURRENT device.

@@ -187,3 +187,40 @@ def test_tiny_workload_abort_set():
     assert list(mask) == [0, 1] and n == 1
     assert np.array_equal(pool.abort_mask.cpu().numpy(), mask)
     assert int(pool.abort_count.item()) == 1
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("what", ["none", "stale_last", "stale_inner", "page_oob", "beyond_table"])
+def test_append_check_one_launch_equals_write_then_check(fp8, what):
+    """fpk_decode_append_check_*: bytes and abort mask equal to the oracle's append followed
+    by its batched check, for clean tables and every kind of bad entry."""
+    ps = 16
+    wl = custom(54, B=6, Hq=8, Hkv=2, ps=ps, prompt_lens=[20, 40, 15, 31, 0, 300], steps=1)
+    pt, ex = wl.page_table.copy(), wl.expected_tags.copy()
+    lens = wl.seq_lens_after(0).copy()
+    r = 1
+    last = (int(lens[r]) - 1) // ps
+    if what == "stale_last":
+        ex[r, last] += np.uint32(3)
+    elif what == "stale_inner":
+        ex[r, 0] -= np.uint32(1)
+    elif what == "page_oob":
+        pt[r, last] = wl.num_pages + 2
+    elif what == "beyond_table":
+        lens[r] = pt.shape[1] * ps + 5
+    wl.page_table, wl.expected_tags = pt, ex
+    pool = DecodePool(wl, fp8=fp8, device=DEV)
+    pool.prefill()
+    pool.set_step(0)
+    pool.seq_lens = to_device(lens, DEV)
+    pool.abort_mask.fill_(9)
+    pool.append_check()
+    torch.cuda.synchronize()
+    ref = oracle_pools(wl, fp8)
+    kn, vn = wl.step_tokens(0)
+    oracle.kv_append(kn, vn, ref, wl.k_scale, wl.v_scale, pt, lens, wl.live_tags, ex, None,
+                     fp8=fp8, Hkv=wl.Hkv, D=wl.D, page_size=ps, num_pages=wl.num_pages)
+    mask, n = oracle.page_tags_validate(pt, ex, lens, wl.live_tags, wl.num_pages, ps)
+    assert np.array_equal(pool.pool_bytes(), ref)
+    assert np.array_equal(pool.abort_mask.cpu().numpy(), mask)
+    assert mask[r] == (0 if what == "none" else 1)
