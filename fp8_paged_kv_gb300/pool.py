@@ -95,12 +95,19 @@ class DecodePool:
         torch.cuda.synchronize(self.device)
 
     def set_step(self, step: int):
-        """Upload decode step `step`'s new K/V rows, query and context lengths."""
+        """Upload decode step `step`'s new K/V rows, query and context lengths.
+        Existing buffers are overwritten in place (captured CUDA graphs keep
+        pointing at them)."""
         kn, vn = self.wl.step_tokens(step)
-        self.k_new = to_device(kn, self.device)
-        self.v_new = to_device(vn, self.device)
-        self.q = to_device(self.wl.step_query(step), self.device)
-        self.seq_lens = to_device(self.wl.seq_lens_after(step), self.device)
+        new = dict(k_new=to_device(kn, self.device), v_new=to_device(vn, self.device),
+                   q=to_device(self.wl.step_query(step), self.device),
+                   seq_lens=to_device(self.wl.seq_lens_after(step), self.device))
+        for name, t in new.items():
+            cur = getattr(self, name)
+            if cur is not None and cur.shape == t.shape and cur.dtype == t.dtype:
+                cur.copy_(t)
+            else:
+                setattr(self, name, t)
 
     def append(self, stream=None, guard: bool = True):
         tags = (self.live_tags, self.expected_tags, self.abort_mask) if guard else (None, None, None)

@@ -1,0 +1,111 @@
+"""Churn + integrity on the GPU: continuous batching with page reallocation and
+injected stale lookups, abort sets bit-exact against the oracle at every step.
+
+The scenario is the integrity evaluation's shape in the Cloudflare write-up
+("La sicurezza della cache KV condivisa diventa una questione di
+produzione", remio.ai: 8192-token inputs, 1000 output tokens): 256 request
+slots, Hq=32/Hkv=8, page size 16; every 50 steps 10 % of the requests finish
+and their pages are reallocated (tags bumped); each step every request's
+lookup goes stale with probability 1 %.  The host ledger decides; the device
+bumps its live tags, writes the step's tokens and checks every mapping in one
+launch, then attends.  The oracle bumps its own copy of the tags and runs its
+own check on the same tables.  Only tags and abort sets are compared here, so
+the cache values are drawn on the device.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_paged_kv_gb300 import (fpk_decode_append_check_fp8, fpk_decode_workspace_bytes,
+                                fpk_kv_prefill_fp8, fpk_page_tags_bump, fpk_paged_decode_attn_fp8)
+from fp8_paged_kv_gb300.pool import to_device
+from workloads.churn import ChurnScenario
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _prefill(sc, kv_pool, k_scale, v_scale, page_table_rows, live, expected_rows, gen, n_tok):
+    """Write `len(rows)` prompts of n_tok tokens each (values drawn on the device)."""
+    R = page_table_rows.shape[0]
+    k = torch.randn(R * n_tok, sc.Hkv, sc.D, device=DEV, generator=gen).to(torch.bfloat16)
+    v = torch.randn(R * n_tok, sc.Hkv, sc.D, device=DEV, generator=gen).to(torch.bfloat16)
+    cu = torch.arange(0, (R + 1) * n_tok, n_tok, dtype=torch.int32, device=DEV)
+    fpk_kv_prefill_fp8(k, v, cu, kv_pool, k_scale, v_scale, page_table_rows, live, expected_rows,
+                       None, Hkv=sc.Hkv, D=sc.D, page_size=sc.ps, num_pages=sc.num_pages)
+
+
+@pytest.mark.parametrize("steps", [1000])
+def test_churn_abort_sets_bit_exact(steps):
+    sc = ChurnScenario(steps=steps)
+    L = sc.ledger
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(5)
+    kv_pool = torch.full((2 * sc.num_pages * sc.Hkv * sc.ps * sc.D,), 0x7F, dtype=torch.uint8,
+                         device=DEV)
+    k_scale = torch.tensor([4.5 / 448], device=DEV)
+    v_scale = torch.tensor([4.5 / 448], device=DEV)
+    live_d = to_device(sc.initial_tags, DEV)
+    live_o = sc.initial_tags.copy()
+    pt_d = to_device(L.page_table, DEV)
+    ex_d = to_device(L.expected, DEV)
+    for r0 in range(0, sc.B, 16):
+        _prefill(sc, kv_pool, k_scale, v_scale, pt_d[r0:r0 + 16], live_d, ex_d[r0:r0 + 16], gen,
+                 sc.prompt)
+    torch.cuda.synchronize()
+    mask_d = torch.zeros(sc.B, dtype=torch.uint8, device=DEV)
+    out = torch.empty(sc.B, sc.Hq, sc.D, device=DEV)
+    lse = torch.empty(sc.B, sc.Hq, device=DEV)
+    ws = torch.zeros(fpk_decode_workspace_bytes(sc.B, sc.Hq, sc.Hkv, sc.D, 0), dtype=torch.uint8,
+                     device=DEV)
+    aborted = ()
+    n_abort = n_admit = 0
+    check_ms = attn_ms = 0.0
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for s in range(steps):
+        ev = sc.next_step(s, aborted)
+        # device: reallocation bumps, table upload, prompts of admitted requests
+        if ev.bump.size:
+            fpk_page_tags_bump(live_d, to_device(ev.bump, DEV), num_pages=sc.num_pages)
+        pt_d.copy_(to_device(L.page_table, DEV))
+        ex_d.copy_(to_device(L.expected, DEV))
+        for r in ev.admitted:
+            _prefill(sc, kv_pool, k_scale, v_scale, pt_d[r:r + 1], live_d, ex_d[r:r + 1], gen,
+                     sc.prompt)
+        lens_d = to_device(ev.lens, DEV)
+        k_new = torch.randn(sc.B, sc.Hkv, sc.D, device=DEV, generator=gen).to(torch.bfloat16)
+        v_new = torch.randn(sc.B, sc.Hkv, sc.D, device=DEV, generator=gen).to(torch.bfloat16)
+        q = torch.randn(sc.B, sc.Hq, sc.D, device=DEV, generator=gen).to(torch.bfloat16)
+        e[0].record()
+        fpk_decode_append_check_fp8(k_new, v_new, kv_pool, k_scale, v_scale, pt_d, lens_d, live_d,
+                                    ex_d, mask_d, Hkv=sc.Hkv, D=sc.D, page_size=sc.ps,
+                                    num_pages=sc.num_pages)
+        e[1].record()
+        fpk_paged_decode_attn_fp8(q, kv_pool, k_scale, v_scale, pt_d, lens_d, mask_d, out, lse, ws,
+                                  Hkv=sc.Hkv, page_size=sc.ps, num_pages=sc.num_pages,
+                                  sm_scale=sc.sm_scale)
+        e[2].record()
+        # oracle: its own tags, its own check on the same tables
+        oracle.page_tags_bump(live_o, ev.bump, sc.num_pages)
+        want, n = oracle.page_tags_validate(L.page_table, L.expected, ev.lens, live_o,
+                                            sc.num_pages, sc.ps)
+        got = mask_d.cpu().numpy()
+        assert np.array_equal(got, want), f"abort set differs at step {s}"
+        assert set(np.flatnonzero(want)) == set(ev.corrupted), f"injected set differs at step {s}"
+        if s % 50 == 0:
+            o = out.cpu().numpy()
+            ls = lse.cpu().numpy()
+            dead = want.astype(bool)
+            assert not o[dead].any() and np.isneginf(ls[dead]).all()
+            assert np.isfinite(o[~dead]).all() and np.isfinite(ls[~dead]).all()
+        check_ms += e[0].elapsed_time(e[1])
+        attn_ms += e[1].elapsed_time(e[2])
+        aborted = tuple(np.flatnonzero(want))
+        n_abort += int(n)
+        n_admit += len(ev.admitted)
+    assert np.array_equal(live_d.cpu().numpy().view(np.uint32), live_o)
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    assert n_abort > 0 and n_admit > 0
+    print(f"churn: {steps} steps, {n_abort} aborts, {n_admit} admissions; "
+          f"write+check {check_ms / steps * 1e3:.1f} us/step, attention {attn_ms / steps * 1e3:.1f} us/step")
