@@ -9,9 +9,11 @@
 // give no kernel design; this one is built for GB300:
 //
 // * Work split.  All (request, kv head) segments are laid end to end as a
-//   list of 16-token tiles; the grid's W CTAs take equal contiguous ranges of
-//   it (one wave with the automatic W), so variable context lengths cost no
-//   tail.  A CTA finds its start with a block scan over seq_lens.
+//   list of 16-token tiles cut into W splits of equal tile count (W = one
+//   wave of CTAs by default), so variable context lengths cost no tail.  At
+//   most one wave of CTAs runs; with more splits than that a CTA takes
+//   consecutive splits in turn without draining its copy pipeline between
+//   them.  A CTA finds its start with a block scan over seq_lens.
 // * Data movement.  Warp 0 is a producer: each of its lanes issues one
 //   cp.async.bulk (TMA) copy of one tile's K block [16 tok][128] and V block
 //   [128][16 tok] -- adjacent in the pool layout, so one copy of 4 KiB (FP8),
@@ -31,7 +33,8 @@
 //   (m, l, O) in shared memory; a CTA that owns a whole segment writes the
 //   final output, otherwise it writes a partial and takes an arrival ticket;
 //   the warp that completes a segment's count merges its partials by
-//   log-sum-exp (one launch per call; nothing ever waits on another CTA).
+//   log-sum-exp in two branch-free passes (one launch per call; nothing ever
+//   waits on another CTA).
 // * Safety.  Every wait is bounded (status word in the workspace); no barrier
 //   without a timeout is used after the prologue.
 #include <atomic>
@@ -94,6 +97,7 @@ struct AttnArgs {
 
 struct Piece {
   int r, h, t0, t1, n;
+  int s;       // split whose partial this piece produces
   int64_t x0;  // global tile index of tile t0
 };
 
@@ -106,10 +110,23 @@ __device__ __forceinline__ int tiles_of(const AttnArgs& a, int r) {
   return tiles_of_request(a.seq_lens, a.abort_mask, r, a.max_pages, a.page_size);
 }
 
-__device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, Piece& p) {
+// Worker w owns global tiles [floor(w T / W), floor((w+1) T / W)); the owner
+// of tile x is floor(((x + 1) W - 1) / T).  With W > T some workers own none.
+__device__ __forceinline__ int worker_of(int64_t x, int64_t T, int W) {
+  return static_cast<int>(((x + 1) * W - 1) / T);
+}
+
+// The next piece of a CTA's tile range: the longest run that stays inside one
+// (request, kv head) segment and one split.
+__device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, int64_t T, Piece& p) {
   if (c.remaining <= 0) return false;
-  const int64_t left = c.n - c.t;
-  const int take = static_cast<int>(left < c.remaining ? left : c.remaining);
+  const int s = worker_of(c.x, T, a.W);
+  const int64_t split_end = (static_cast<int64_t>(s) + 1) * T / a.W;
+  int64_t take64 = c.n - c.t;
+  if (c.remaining < take64) take64 = c.remaining;
+  if (split_end - c.x < take64) take64 = split_end - c.x;
+  const int take = static_cast<int>(take64);
+  p.s = s;
   p.r = c.r;
   p.h = c.h;
   p.t0 = c.t;
@@ -132,13 +149,6 @@ __device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, Piece& 
   }
   return true;
 }
-
-// Worker w owns global tiles [floor(w T / W), floor((w+1) T / W)); the owner
-// of tile x is floor(((x + 1) W - 1) / T).  With W > T some workers own none.
-__device__ __forceinline__ int worker_of(int64_t x, int64_t T, int W) {
-  return static_cast<int>(((x + 1) * W - 1) / T);
-}
-
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
@@ -167,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   int* s_stage_fault = reinterpret_cast<int*>(bars + 2 * C::kStages + 3);
 
   __shared__ int64_t s_warp_sum[kThreads / 32];
-  __shared__ int64_t s_total;
   __shared__ int s_start[4];
   __shared__ int s_last;
 
@@ -202,11 +211,15 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   }
   const int64_t excl = before + incl - mine;
   const int64_t T = total * a.Hkv;
-  const int64_t b0 = static_cast<int64_t>(w) * T / a.W;
-  const int64_t b1 = static_cast<int64_t>(w + 1) * T / a.W;
+  // this CTA runs splits [s0, s1) one after another: tiles [b0, b1)
+  const int nctas = static_cast<int>(gridDim.x);
+  const int64_t s0 = static_cast<int64_t>(w) * a.W / nctas;
+  const int64_t s1 = static_cast<int64_t>(w + 1) * a.W / nctas;
+  const int64_t b0 = s0 * T / a.W;
+  const int64_t b1 = s1 * T / a.W;
   // requests that read nothing (empty, aborted, over-long) get out = 0 and
   // lse = -inf; the CTAs share this round-robin
-  for (int r = w; r < a.B; r += a.W) {
+  for (int r = w; r < a.B; r += nctas) {
     if (tiles_of(a, r) == 0) {
       float* orow = a.out + static_cast<int64_t>(r) * a.Hq * kDim;
       for (int i = tid; i < a.Hq * kDim; i += kThreads) orow[i] = 0.f;
@@ -231,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       base += span;
     }
   }
-  if (tid == 0) s_total = T;
   // barriers
   const uint32_t full0 = smem_addr(bars);
   const uint32_t empty0 = full0 + 8 * C::kStages;
@@ -281,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     Piece p;
     uint32_t j = 0;  // stages issued so far
     bool ok = true;
-    while (ok && next_piece(cur, a, p)) {
+    while (ok && next_piece(cur, a, T, p)) {
       const int32_t* ptrow = a.page_table + static_cast<int64_t>(p.r) * a.max_pages;
       const int nst = (p.t1 - p.t0 + 1) >> 1;
       auto load_id = [&](int k0) {
@@ -380,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   bool ok = true;
   const float kNegInf = -INFINITY;
 
-  while (ok && next_piece(cur, a, p)) {
+  while (ok && next_piece(cur, a, T, p)) {
     const int ntiles = p.t1 - p.t0;
     const int L = __ldg(a.seq_lens + p.r);
     // ---- query fragments (B operand of S^T = K Q^T), heads of this kv group
@@ -674,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         a.out[row * kDim + d] = dead ? 0.f : acc * vmul / wsum;
         if (d == 0 && a.lse != nullptr) a.lse[row] = dead ? kNegInf : (M + __log2f(wsum)) * kLn2;
       } else {
-        const int64_t slot = static_cast<int64_t>(seg) + w;
+        const int64_t slot = static_cast<int64_t>(seg) + p.s;
         a.part_o[(slot * a.G + hd) * kDim + d] = acc * vmul;
         if (d == 0) a.part_ml[slot * a.G + hd] = dead ? make_float2(kNegInf, -1.f) : make_float2(M, wsum);
       }
@@ -689,11 +701,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       bool got = mbar_wait(cbar, cphase & 1, a.status);
       ++cphase;
       if (!__all_sync(kFull, got)) break;
-      const int64_t T = s_total;
       const int64_t xseg = p.x0 - p.t0;  // global index of the segment's first tile
       const int w0 = worker_of(xseg, T, a.W);
       const int w1 = worker_of(xseg + p.n - 1, T, a.W);
-      // CTAs holding a piece of this segment: all of w0..w1 when every worker
+      // splits holding a piece of this segment: all of w0..w1 when every split
       // owns tiles (T >= W), else one per tile (the i-th is the owner of tile i)
       const bool dense = T >= a.W;
       const int nsl = dense ? w1 - w0 + 1 : p.n;
@@ -708,38 +719,53 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       if (!__all_sync(kFull, got)) break;
       if (s_last) {
         __threadfence();
-        // one pass of online log-sum-exp over the contributing slots; thread ct
-        // owns dim d = ct of every head of the group
+        // Two passes over the contributing slots, neither with a branch on a
+        // loaded value, so the loads of many slots are in flight at once:
+        // first each head's largest partial log-sum-exp and the fault flag,
+        // then the rescaled sums.  Thread ct owns dim d = ct of every head.
         const int d = ct;
-        float M[kGroupMax], Wl[kGroupMax], acc[kGroupMax];
+        float M[kGroupMax];
         bool dead = false;
 #pragma unroll
-        for (int hd = 0; hd < kGroupMax; ++hd) M[hd] = kNegInf, Wl[hd] = 0.f, acc[hd] = 0.f;
+        for (int hd = 0; hd < kGroupMax; ++hd) M[hd] = kNegInf;
 #pragma unroll 4
         for (int i = 0; i < nsl; ++i) {
-          const int k = dense ? w0 + i : worker_of(xseg + i, T, a.W);
-          const int64_t slot = static_cast<int64_t>(seg) + k;
+          const int64_t slot = static_cast<int64_t>(seg) + (dense ? w0 + i : worker_of(xseg + i, T, a.W));
+#pragma unroll
+          for (int hd = 0; hd < kGroupMax; ++hd) {
+            if (hd < a.G) {
+              const float2 ml = __ldcg(a.part_ml + slot * a.G + hd);
+              M[hd] = fmaxf(M[hd], ml.x);
+              dead |= ml.y < 0.f;
+            }
+          }
+        }
+        float Wl[kGroupMax], acc[kGroupMax];
+#pragma unroll
+        for (int hd = 0; hd < kGroupMax; ++hd) {
+          Wl[hd] = 0.f;
+          acc[hd] = 0.f;
+          if (M[hd] == kNegInf) M[hd] = 0.f;  // no live slot: every weight below is 0
+        }
+#pragma unroll 2
+        for (int i = 0; i < nsl; ++i) {
+          const int64_t slot = static_cast<int64_t>(seg) + (dense ? w0 + i : worker_of(xseg + i, T, a.W));
 #pragma unroll
           for (int hd = 0; hd < kGroupMax; ++hd) {
             if (hd < a.G) {
               const float2 ml = __ldcg(a.part_ml + slot * a.G + hd);
               const float ov = __ldcg(a.part_o + (slot * a.G + hd) * kDim + d);
-              dead |= ml.y < 0.f;
-              if (ml.x != kNegInf) {
-                const float mn = fmaxf(M[hd], ml.x);
-                const float fo = M[hd] == kNegInf ? 0.f : fast_exp2(M[hd] - mn);
-                const float fk = fast_exp2(ml.x - mn);
-                Wl[hd] = Wl[hd] * fo + ml.y * fk;
-                acc[hd] = acc[hd] * fo + ov * fk;
-                M[hd] = mn;
-              }
+              const bool live = ml.x != kNegInf;  // empty or faulted slots weigh 0
+              const float f = fast_exp2(ml.x - M[hd]);
+              Wl[hd] = live ? fmaf(ml.y, f, Wl[hd]) : Wl[hd];
+              acc[hd] = live ? fmaf(ov, f, acc[hd]) : acc[hd];
             }
           }
         }
 #pragma unroll
         for (int hd = 0; hd < kGroupMax; ++hd) {
           if (hd < a.G) {
-            const bool dh = dead || M[hd] == kNegInf;
+            const bool dh = dead || Wl[hd] == 0.f;
             const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
             a.out[row * kDim + d] = dh ? 0.f : acc[hd] / Wl[hd];
             if (d == 0 && a.lse != nullptr) a.lse[row] = dh ? kNegInf : (M[hd] + __log2f(Wl[hd])) * kLn2;
@@ -831,12 +857,11 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
     return FPK_EINVAL;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FPK_ECUDA;
-  if (prepare_kernel<kFp8>(dev) <= 0) return FPK_ECUDA;
-  int W = num_splits;
-  if (W == 0) {
-    W = device_sm_count(dev) * prepare_kernel<kFp8>(dev);
-    if (W <= 0) return FPK_ECUDA;
-  }
+  const int per_sm = prepare_kernel<kFp8>(dev);
+  const int wave = device_sm_count(dev) * per_sm;  // CTAs resident at once
+  if (per_sm <= 0 || wave <= 0) return FPK_ECUDA;
+  const int W = num_splits == 0 ? wave : num_splits;
+  const int ctas = W < wave ? W : wave;  // more splits than that: a CTA runs several in turn
   const int G = Hq / Hkv;
   const WsLayout l = layout(B, Hkv, G, W);
   if (workspace_bytes < l.total) return FPK_ENOSPC;
@@ -865,7 +890,7 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
   a.W = W;
   a.sm_scale_log2 = sm_scale * kLog2e;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  paged_decode_split_kernel<kFp8><<<W, kThreads, Cfg<kFp8>::kSmemBytes, s>>>(a);
+  paged_decode_split_kernel<kFp8><<<ctas, kThreads, Cfg<kFp8>::kSmemBytes, s>>>(a);
   return checked_launch_status();
 }
 

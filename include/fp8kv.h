@@ -247,9 +247,11 @@ size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  *               that share a workspace must not overlap on the GPU.
  *   num_splits: number of split-KV work units the batch's KV tiles are
  *               divided into (balanced by tile count across all requests and
- *               kv heads); 0 = automatic (fills the GPU once).  With equal
+ *               kv heads); each split's partial enters the log-sum-exp
+ *               combine.  0 = automatic (one wave of CTAs).  With equal
  *               context lengths, num_splits = S * B * Hkv gives exactly S
- *               splits per (request, kv head).
+ *               splits per (request, kv head).  At most one wave of CTAs is
+ *               launched; beyond that a CTA runs several splits in turn.
  *   sm_scale  : softmax scale (1/sqrt(D) for standard attention).
  */
 int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* kv_pool,
