@@ -88,7 +88,8 @@ struct AttnArgs {
   float* out;
   float* lse;
   uint32_t* status;
-  int* seg_count;  // per-segment arrival tickets, zero between calls
+  int* seg_count;    // per-segment arrival tickets, zero between calls
+  int* group_count;  // per-group arrival tickets (indexed by slot), zero between calls
   float2* part_ml;
   float* part_o;
   int B, Hq, Hkv, G, page_size, num_pages, max_pages, W;
@@ -99,6 +100,14 @@ struct Piece {
   int r, h, t0, t1, n;
   int s;       // split whose partial this piece produces
   int64_t x0;  // global tile index of tile t0
+};
+
+// Slots of the members i0, i0 + stride, ... of one segment's partials: member
+// i is split w0 + i when every split owns tiles, else the owner of tile i.
+struct Members {
+  int64_t seg, xseg;
+  int w0, i0, stride;
+  bool dense;
 };
 
 struct Cursor {
@@ -389,8 +398,195 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   uint32_t jbase = 0;
   uint32_t piece_idx = 0;
   uint32_t cphase = 0;  // completed phases of cbar
+  const int ct_all = c * 32 + lane;  // consumer thread 0..127
   bool ok = true;
   const float kNegInf = -INFINITY;
+  // barrier of the four consumer warps (bounded wait); false if it gave up
+  auto consumer_sync = [&]() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cbar);
+    const bool got = mbar_wait(cbar, cphase & 1, a.status);
+    ++cphase;
+    return __all_sync(kFull, got);
+  };
+  // Arrival ticket on a counter in global memory: every partial write of this
+  // CTA is fenced first; returns 1 for the arrival that completes `count`,
+  // 0 for the others, -1 if a barrier gave up.  Nothing ever waits on another
+  // CTA.
+  auto ticket = [&](int* ctr, int count) -> int {
+    __threadfence();
+    if (!consumer_sync()) return -1;
+    if (ct_all == 0) {
+      s_last = atomicAdd(ctr, 1) == count - 1;
+      __threadfence();
+    }
+    if (!consumer_sync()) return -1;
+    return s_last;
+  };
+  // Log-sum-exp of n partials (unnormalised sums with their (M, l) pairs in
+  // the log2 domain), taken from slots slot_of(k) for k < n, a chunk of slots
+  // at a time: the chunk's (m, l) pairs are staged in shared memory, one
+  // thread per head turns them into weights e^(m - M) against the running
+  // maximum M (rescaling the running sums when M grows), then every thread
+  // accumulates weight x partial for one float4 of dims of two heads.  Head
+  // indices past the group are clamped rather than branched on, so the loads
+  // of several slots are in flight together.  The result goes to the final
+  // output rows of (r, h) when dst < 0, else, as a partial, to slot dst.
+  auto combine = [&](const Members& mb, int n, int r, int h, int64_t dst) -> bool {
+    auto slot_of = [&](int k) -> int64_t {
+      const int i = mb.i0 + k * mb.stride;
+      return mb.seg + (mb.dense ? mb.w0 + i : worker_of(mb.xseg + i, T, a.W));
+    };
+    float2* s_w = reinterpret_cast<float2*>(s_o);
+    constexpr int kChunk = kConsumerWarps * kGroupMax * kMergeStride / (2 * kGroupMax);
+    float* s_M = s_m;              // running maximum per head
+    float* s_r = s_m + kGroupMax;  // rescale of the running sums by this chunk
+    float* s_W = s_l;              // running sum of weights per head
+    int* s_dead = s_wfault;        // some split faulted
+    const int ct = ct_all;
+    const int d4 = ct & 31;
+    const int hq0 = ct >> 5;  // heads hq0 and hq0 + 4
+    const int hh0 = min(hq0, a.G - 1);
+    const int hh1 = min(hq0 + 4, a.G - 1);
+    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+    __threadfence();
+    if (ct < kGroupMax) {
+      s_M[ct] = kNegInf;
+      s_W[ct] = 0.f;
+    }
+    if (ct == 0) *s_dead = 0;
+    for (int c0 = 0; c0 < n; c0 += kChunk) {
+      const int nc = min(kChunk, n - c0);
+      for (int e = ct; e < nc * a.G; e += kConsumerWarps * 32) {
+        const int i = e / a.G;
+        const int hd = e - i * a.G;
+        s_w[i * kGroupMax + hd] = __ldcg(a.part_ml + slot_of(c0 + i) * a.G + hd);
+      }
+      if (!consumer_sync()) return false;
+      if (ct < a.G) {
+        float mc = kNegInf;
+        bool dd = false;
+        for (int i = 0; i < nc; ++i) {
+          const float2 ml = s_w[i * kGroupMax + ct];
+          mc = fmaxf(mc, ml.x);
+          dd |= ml.y < 0.f;
+        }
+        const float mo = s_M[ct];
+        const float mn = fmaxf(mo, mc);
+        const float rs = mo == kNegInf ? 0.f : fast_exp2(mo - mn);
+        float wsum = s_W[ct] * rs;
+        for (int i = 0; i < nc; ++i) {
+          const float2 ml = s_w[i * kGroupMax + ct];
+          const float f = ml.x == kNegInf ? 0.f : fast_exp2(ml.x - mn);
+          wsum = fmaf(ml.y, f, wsum);
+          s_w[i * kGroupMax + ct].x = f;
+        }
+        s_M[ct] = mn;
+        s_r[ct] = rs;
+        s_W[ct] = wsum;
+        if (dd) *s_dead = 1;
+      }
+      if (!consumer_sync()) return false;
+      {
+        const float r0 = s_r[hh0], r1 = s_r[hh1];
+        acc0 = make_float4(acc0.x * r0, acc0.y * r0, acc0.z * r0, acc0.w * r0);
+        acc1 = make_float4(acc1.x * r1, acc1.y * r1, acc1.z * r1, acc1.w * r1);
+      }
+#pragma unroll 2
+      for (int i = 0; i < nc; ++i) {
+        const float4* po = reinterpret_cast<const float4*>(a.part_o + slot_of(c0 + i) * a.G * kDim);
+        const float4 v0 = __ldcg(po + hh0 * (kDim / 4) + d4);
+        const float4 v1 = __ldcg(po + hh1 * (kDim / 4) + d4);
+        const float f0 = s_w[i * kGroupMax + hh0].x;
+        const float f1 = s_w[i * kGroupMax + hh1].x;
+        acc0 = make_float4(fmaf(v0.x, f0, acc0.x), fmaf(v0.y, f0, acc0.y), fmaf(v0.z, f0, acc0.z),
+                           fmaf(v0.w, f0, acc0.w));
+        acc1 = make_float4(fmaf(v1.x, f1, acc1.x), fmaf(v1.y, f1, acc1.y), fmaf(v1.z, f1, acc1.z),
+                           fmaf(v1.w, f1, acc1.w));
+      }
+      // every thread is done with this chunk's weights before the next overwrites them
+      if (c0 + kChunk < n && !consumer_sync()) return false;
+    }
+    const bool dead = *s_dead != 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int hd = hq0 + 4 * j;
+      if (hd < a.G) {
+        const float W = s_W[hd];
+        const float4 av = j == 0 ? acc0 : acc1;
+        if (dst < 0) {
+          const bool dh = dead || W == 0.f;
+          const float iw = dh ? 0.f : 1.f / W;
+          const int64_t row = static_cast<int64_t>(r) * a.Hq + h * a.G + hd;
+          reinterpret_cast<float4*>(a.out + row * kDim)[d4] =
+              make_float4(av.x * iw, av.y * iw, av.z * iw, av.w * iw);
+          if (d4 == 0 && a.lse != nullptr) a.lse[row] = dh ? kNegInf : (s_M[hd] + __log2f(W)) * kLn2;
+        } else {
+          // each thread overwrites only the dims it read itself; the (m, l)
+          // pairs were all read before the last barrier
+          reinterpret_cast<float4*>(a.part_o + (dst * a.G + hd) * kDim)[d4] = av;
+          if (d4 == 0)
+            a.part_ml[dst * a.G + hd] = dead ? make_float2(kNegInf, -1.f)
+                                             : make_float2(W == 0.f ? kNegInf : s_M[hd], W);
+        }
+      }
+    }
+    return true;
+  };
+  // A piece that is not a whole segment has written its partial to its slot.
+  // Members of the segment are numbered i = 0..nsl-1 in tile order.  Up to
+  // kDirect members, the arrival that completes the segment's count combines
+  // them all.  Beyond that the members form groups of K ~ sqrt(nsl): the
+  // arrival completing a group folds it into the slot of its first member,
+  // and the group completing the segment's count combines the group results,
+  // so no CTA reads more than about max(K, nsl / K) partials.
+  auto publish_partial = [&](const Piece& p, int seg) -> bool {
+    constexpr int kDirect = 16;
+    const int64_t xseg = p.x0 - p.t0;  // global index of the segment's first tile
+    const int w0 = worker_of(xseg, T, a.W);
+    const int w1 = worker_of(xseg + p.n - 1, T, a.W);
+    // splits holding a piece of this segment: all of w0..w1 when every split
+    // owns tiles (T >= W), else one per tile (the i-th is the owner of tile i)
+    const bool dense = T >= a.W;
+    const int nsl = dense ? w1 - w0 + 1 : p.n;
+    const int me = dense ? p.s - w0 : p.t0;
+    Members mb;
+    mb.seg = seg;
+    mb.xseg = xseg;
+    mb.w0 = w0;
+    mb.dense = dense;
+    mb.i0 = 0;
+    mb.stride = 1;
+    int* ctr = a.seg_count + seg;
+    int n = nsl;
+    int64_t dst = -1;
+    int K = 1, ng = 1;
+    if (nsl > kDirect) {
+      K = static_cast<int>(sqrtf(static_cast<float>(nsl)));
+      while (K * K < nsl) ++K;
+      ng = (nsl + K - 1) / K;
+      const int gi = me / K;
+      mb.i0 = gi * K;
+      n = min(K, nsl - mb.i0);
+      dst = seg + (dense ? w0 + mb.i0 : worker_of(xseg + mb.i0, T, a.W));
+      ctr = a.group_count + dst;
+    }
+    for (;;) {
+      const int last = ticket(ctr, n);
+      if (last < 0) return false;
+      if (last == 0) return true;
+      if (!combine(mb, n, p.r, p.h, dst)) return false;
+      if (ct_all == 0) *ctr = 0;  // ready for the next call
+      if (dst < 0) return true;
+      // the group is folded into the slot of its first member: on to the
+      // segment's count of groups
+      ctr = a.seg_count + seg;
+      n = ng;
+      dst = -1;
+      mb.i0 = 0;
+      mb.stride = K;
+    }
+  };
 
   while (ok && next_piece(cur, a, T, p)) {
     const int ntiles = p.t1 - p.t0;
@@ -662,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     }
     const int seg = p.r * a.Hkv + p.h;
     const bool whole = p.t0 == 0 && p.t1 == p.n;
-    const int ct = c * 32 + lane;
+    const int ct = ct_all;
     int anyfault = 0;
 #pragma unroll
     for (int k = 0; k < kConsumerWarps; ++k) anyfault |= s_wfault[k];
@@ -691,89 +887,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         if (d == 0) a.part_ml[slot * a.G + hd] = dead ? make_float2(kNegInf, -1.f) : make_float2(M, wsum);
       }
     }
-    if (!whole) {
-      // Arrival ticket per CTA: the CTA that completes the count for this
-      // segment merges every contributing CTA's partial (nothing ever waits on
-      // another CTA).  All partial writes of this CTA are fenced first.
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cbar);
-      bool got = mbar_wait(cbar, cphase & 1, a.status);
-      ++cphase;
-      if (!__all_sync(kFull, got)) break;
-      const int64_t xseg = p.x0 - p.t0;  // global index of the segment's first tile
-      const int w0 = worker_of(xseg, T, a.W);
-      const int w1 = worker_of(xseg + p.n - 1, T, a.W);
-      // splits holding a piece of this segment: all of w0..w1 when every split
-      // owns tiles (T >= W), else one per tile (the i-th is the owner of tile i)
-      const bool dense = T >= a.W;
-      const int nsl = dense ? w1 - w0 + 1 : p.n;
-      if (ct == 0) {
-        s_last = atomicAdd(a.seg_count + seg, 1) == nsl - 1;
-        __threadfence();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cbar);
-      got = mbar_wait(cbar, cphase & 1, a.status);
-      ++cphase;
-      if (!__all_sync(kFull, got)) break;
-      if (s_last) {
-        __threadfence();
-        // Two passes over the contributing slots, neither with a branch on a
-        // loaded value, so the loads of many slots are in flight at once:
-        // first each head's largest partial log-sum-exp and the fault flag,
-        // then the rescaled sums.  Thread ct owns dim d = ct of every head.
-        const int d = ct;
-        float M[kGroupMax];
-        bool dead = false;
-#pragma unroll
-        for (int hd = 0; hd < kGroupMax; ++hd) M[hd] = kNegInf;
-#pragma unroll 4
-        for (int i = 0; i < nsl; ++i) {
-          const int64_t slot = static_cast<int64_t>(seg) + (dense ? w0 + i : worker_of(xseg + i, T, a.W));
-#pragma unroll
-          for (int hd = 0; hd < kGroupMax; ++hd) {
-            if (hd < a.G) {
-              const float2 ml = __ldcg(a.part_ml + slot * a.G + hd);
-              M[hd] = fmaxf(M[hd], ml.x);
-              dead |= ml.y < 0.f;
-            }
-          }
-        }
-        float Wl[kGroupMax], acc[kGroupMax];
-#pragma unroll
-        for (int hd = 0; hd < kGroupMax; ++hd) {
-          Wl[hd] = 0.f;
-          acc[hd] = 0.f;
-          if (M[hd] == kNegInf) M[hd] = 0.f;  // no live slot: every weight below is 0
-        }
-#pragma unroll 2
-        for (int i = 0; i < nsl; ++i) {
-          const int64_t slot = static_cast<int64_t>(seg) + (dense ? w0 + i : worker_of(xseg + i, T, a.W));
-#pragma unroll
-          for (int hd = 0; hd < kGroupMax; ++hd) {
-            if (hd < a.G) {
-              const float2 ml = __ldcg(a.part_ml + slot * a.G + hd);
-              const float ov = __ldcg(a.part_o + (slot * a.G + hd) * kDim + d);
-              const bool live = ml.x != kNegInf;  // empty or faulted slots weigh 0
-              const float f = fast_exp2(ml.x - M[hd]);
-              Wl[hd] = live ? fmaf(ml.y, f, Wl[hd]) : Wl[hd];
-              acc[hd] = live ? fmaf(ov, f, acc[hd]) : acc[hd];
-            }
-          }
-        }
-#pragma unroll
-        for (int hd = 0; hd < kGroupMax; ++hd) {
-          if (hd < a.G) {
-            const bool dh = dead || Wl[hd] == 0.f;
-            const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
-            a.out[row * kDim + d] = dh ? 0.f : acc[hd] / Wl[hd];
-            if (d == 0 && a.lse != nullptr) a.lse[row] = dh ? kNegInf : (M[hd] + __log2f(Wl[hd])) * kLn2;
-          }
-        }
-        if (ct == 0) a.seg_count[seg] = 0;  // ready for the next call
-      }
-    }
+    if (!whole && !publish_partial(p, seg)) break;
     __syncwarp();
     if (lane == 0) mbar_arrive(merge_free);
     ++piece_idx;
@@ -807,7 +921,7 @@ int prepare_kernel(int dev) {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t seg_count, part_ml, part_o, total;
+  size_t seg_count, group_count, part_ml, part_o, total;
 };
 
 WsLayout layout(int64_t B, int64_t Hkv, int64_t G, int64_t W) {
@@ -815,7 +929,8 @@ WsLayout layout(int64_t B, int64_t Hkv, int64_t G, int64_t W) {
   const int64_t segs = B * Hkv;
   const int64_t slots = segs + W;
   l.seg_count = 256;
-  l.part_ml = l.seg_count + align256(static_cast<size_t>(segs) * sizeof(int));
+  l.group_count = l.seg_count + align256(static_cast<size_t>(segs) * sizeof(int));
+  l.part_ml = l.group_count + align256(static_cast<size_t>(slots) * sizeof(int));
   l.part_o = l.part_ml + align256(static_cast<size_t>(slots * G) * sizeof(float2));
   l.total = l.part_o + align256(static_cast<size_t>(slots * G * kDim) * sizeof(float));
   return l;
@@ -878,6 +993,7 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
   a.lse = lse;
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.seg_count = reinterpret_cast<int*>(ws + l.seg_count);
+  a.group_count = reinterpret_cast<int*>(ws + l.group_count);
   a.part_ml = reinterpret_cast<float2*>(ws + l.part_ml);
   a.part_o = reinterpret_cast<float*>(ws + l.part_o);
   a.B = B;

@@ -239,7 +239,7 @@ size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  *   out       : float [B][Hq][D];  lse: float [B][Hq], nullable
  *   workspace : >= fpk_decode_workspace_bytes(...) bytes, 256-byte aligned,
  *               owned by the caller.  Zero it ONCE after allocating: it holds
- *               per-segment arrival counters that every call leaves at zero
+ *               arrival counters that every call leaves at zero
  *               again, split partials, and in its first 4 bytes a status word
  *               the kernel sets to nonzero (and never clears) if a bounded
  *               internal wait gave up; read it with fpk_decode_status and

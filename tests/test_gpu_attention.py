@@ -61,7 +61,7 @@ def test_small_ragged(fp8, G, ps):
 
 
 @pytest.mark.parametrize("fp8", [True, False])
-@pytest.mark.parametrize("num_splits", [1, 2, 5, 37, 300, 4096])
+@pytest.mark.parametrize("num_splits", [1, 2, 5, 37, 61, 200, 300, 4096])
 def test_split_counts(fp8, num_splits):
     lens = [700, 33, 0, 1025, 64, 5]
     wl = custom(70 + num_splits, B=len(lens), Hq=16, Hkv=2, ps=16, prompt_lens=lens, steps=0)
