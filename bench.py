@@ -459,9 +459,11 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         if g_seq is None:
+            timed_steps = args.steps
             ms_step = time_graph(g_step, args.steps, args.warmup)
         else:
             reps = max(1, args.steps // seq_steps)
+            timed_steps = reps * seq_steps
             ms_step = time_graph(g_seq, reps, max(1, args.warmup // seq_steps)) / seq_steps
     barrier(world)
     ms_step = max_over_ranks(ms_step, world)
@@ -510,10 +512,10 @@ def main():
         "e2e": {"value": live * world / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
     }
-    # per replayed step: append, validate, attention (the combine is inside the attention kernel)
-    launches_per_step = 3
-    if args.steps:
-        out["gpu_launches"] = launches_per_step * args.steps
+    # per timed step: the cache write + tag check launch and the attention launch
+    # (the split combine runs inside the attention kernel)
+    launches_per_step = 2
+    out["gpu_launches"] = launches_per_step * timed_steps
     del pool
     torch.cuda.empty_cache()
 
