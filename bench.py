@@ -374,6 +374,52 @@ def capture_steps_sequence(pool, nsteps: int):
     return g, (K, V, Q, lens)
 
 
+def time_prefill(pool, reps: int = 5):
+    """The bulk prompt write into the FP8 pages and the device amax -> scale
+    reduction over K and V, with the whole prompt resident on the device.  The
+    write reuses the pool's own scales, so the cache contents do not change."""
+    import fp8_paged_kv_gb300 as fpk
+    from fp8_paged_kv_gb300.pool import to_device
+    wl = pool.wl
+    dev = pool.device
+    k = to_device(wl.k_prompt, dev)
+    v = to_device(wl.v_prompt, dev)
+    cu = to_device(wl.cu_prompt.astype(np.int32), dev)
+    ks = torch.empty(1, dtype=torch.float32, device=dev)
+    vs = torch.empty(1, dtype=torch.float32, device=dev)
+    scratch = torch.zeros(2, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def write():
+        fpk.fpk_kv_prefill_fp8(k, v, cu, pool.kv_pool, pool.k_scale, pool.v_scale, pool.page_table,
+                               pool.live_tags, pool.expected_tags, None, **pool.kw)
+
+    def amax():
+        fpk.fpk_amax_scale_bf16(k, ks, scratch)
+        fpk.fpk_amax_scale_bf16(v, vs, scratch)
+
+    res = []
+    for fn in (write, amax):
+        fn()
+        torch.cuda.synchronize(dev)
+        t = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            torch.cuda.synchronize(dev)
+            t.append(a.elapsed_time(b))
+        res.append(statistics.median(t))
+    n = int(wl.k_prompt.size)  # bf16 elements of K (and of V)
+    write_bytes = 2 * n * 2 + 2 * n          # read K, V bf16; write their e4m3 codes
+    amax_bytes = 2 * n * 2                   # read K and V
+    del k, v
+    return {"tokens": int(wl.cu_prompt[-1]), "write_us": res[0] * 1e3,
+            "write_gbs": write_bytes / (res[0] * 1e-3) / 1e9, "amax_scale_us": res[1] * 1e3,
+            "amax_scale_gbs": amax_bytes / (res[1] * 1e-3) / 1e9}
+
+
 def time_e2e(pool, steps: int, warmup: int):
     """Same step through the public API with host buffers: pinned H2D of the step's
     inputs (q, new K/V rows, context lengths), the step, D2H of out/lse/abort mask."""
@@ -487,6 +533,7 @@ def main():
 
     e2e_ms, h2d, d2h = time_e2e(pool, max(args.steps // 4, 20), 3)
     e2e_ms = max_over_ranks(e2e_ms, world)
+    prefill = time_prefill(pool)
 
     abytes = attention_bytes(wl, 0, True)
     peak, peak_kind = measured_peaks()
@@ -511,6 +558,7 @@ def main():
         "gpu_launches": None, "clocks": clk.summary(),
         "e2e": {"value": live * world / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "prefill": prefill,
     }
     # per timed step: the cache write + tag check launch and the attention launch
     # (the split combine runs inside the attention kernel)

@@ -43,6 +43,7 @@ SIGNATURES = {
     "fpk_kv_prefill_bf16": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _I32, _P, _P, _P,
                                            _I32, _I32, _I32, _I32, _I32, _P]),
     "fpk_quantize_e4m3": (ctypes.c_int, [_P, _P, _P, _I64, _P]),
+    "fpk_amax_scale_bf16": (ctypes.c_int, [_P, _I64, _P, _P, _P]),
     "fpk_page_tags_bump": (ctypes.c_int, [_P, _P, _I32, _I32, _P]),
     "fpk_page_tags_validate": (ctypes.c_int, [_P, _P, _P, _I32, _P, _I32, _I32, _I32, _P, _P, _P]),
     "fpk_decode_append_check_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P,
@@ -210,6 +211,12 @@ def fpk_quantize_e4m3(x, scale, out, stream=None):
     _check(load_library().fpk_quantize_e4m3(_ptr(x, _F32, "x"), _ptr(scale, _F32, "scale"),
                                             _ptr(out, _U8, "out"), x.numel(), _stream(stream)),
            "fpk_quantize_e4m3")
+
+
+def fpk_amax_scale_bf16(x, scale, scratch, stream=None):
+    _check(load_library().fpk_amax_scale_bf16(_ptr(x, _BF16_LIKE, "x"), x.numel(),
+                                              _ptr(scale, _F32, "scale"), _ptr(scratch, _TAGS, "scratch"),
+                                              _stream(stream)), "fpk_amax_scale_bf16")
 
 
 def fpk_page_tags_bump(live_tags, pages, *, num_pages, stream=None):

@@ -158,6 +158,22 @@ int fpk_kv_prefill_bf16(const void* k, const void* v, const int32_t* cu_seqlens,
 int fpk_quantize_e4m3(const float* x, const float* scale, uint8_t* out, int64_t n, void* stream);
 
 /*
+ * Per-tensor scale of a bf16 tensor for the e4m3 cache: *scale = amax / 448,
+ * amax = max |x[i]| over the finite elements (infinities and NaNs are
+ * skipped); *scale = 1 when amax == 0 or n == 0.  The division is one IEEE
+ * fp32 division.  The pages state only that the cache holds e4m3 values
+ * ("Cosa ha cambiato Cloudflare per Kimi e GLM", remio.ai); one fp32 scale per
+ * tensor equal to amax / 448 is this library's reading.  Use it on a prompt's
+ * K (resp. V) before fpk_kv_prefill_fp8, which reads the scale on the device.
+ *   x       : bf16 [n] (device, 16-byte aligned)
+ *   scale   : float [1] (device, written)
+ *   scratch : uint32 [2] (device), caller-owned; the call zeroes it first.
+ *             Calls that share scratch must not overlap on the GPU.
+ * Result is bit-exact (the max is an integer max of bit patterns).
+ */
+int fpk_amax_scale_bf16(const void* x, int64_t n, float* scale, uint32_t* scratch, void* stream);
+
+/*
  * Page reallocation: live_tags[pages[i]] += 1 (mod 2^32) for i < n.
  * Source: "Cosa ha cambiato..." -- a page's tag changes every time the page is
  * reallocated; "La sicurezza della cache KV condivisa..." -- the tags behave

@@ -61,6 +61,8 @@ def _load():
             lib.orc_quantize_bf16.restype = ctypes.c_uint8
             lib.orc_quantize_bf16.argtypes = [ctypes.c_uint16, _F]
             lib.orc_quantize_bf16_array.argtypes = [_P, _I64, _F, _P]
+            lib.orc_amax_scale_bf16.restype = _F
+            lib.orc_amax_scale_bf16.argtypes = [_P, _I64]
             lib.orc_kv_append.argtypes = [_P, _P, _I, _P, _F, _F, _P, _I, _P,
                                           _P, _P, _P, _I, _I, _I, _I, _I]
             lib.orc_kv_prefill.argtypes = [_P, _P, _P, _I, _P, _F, _F, _P, _I,
@@ -112,6 +114,12 @@ def quantize_bf16(xbits, scale: float) -> np.ndarray:
     out = np.empty(xb.shape, np.uint8)
     _load().orc_quantize_bf16_array(_ptr(xb), xb.size, float(np.float32(scale)), _ptr(out))
     return out
+
+
+def amax_scale_bf16(xbits) -> np.float32:
+    """Per-tensor scale amax / 448 over the finite bf16 elements (1 if amax = 0)."""
+    xb = _c(xbits, np.uint16)
+    return np.float32(_load().orc_amax_scale_bf16(_ptr(xb), xb.size))
 
 
 # --------------------------------------------------------------------------

@@ -154,6 +154,31 @@ void orc_quantize_bf16_array(const uint16_t *xbits, int64_t n, float scale, uint
         out[i] = orc_quantize_bf16(xbits[i], scale);
 }
 
+/*
+ * Per-tensor scale of the e4m3 cache: amax / 448 over the finite elements of a
+ * bf16 tensor, 1 when there is no nonzero finite element.  The pages name the
+ * e4m3 format only ("Cosa ha cambiato Cloudflare per Kimi e GLM"); one fp32
+ * scale per tensor with the tensor's largest magnitude mapped to the largest
+ * finite code (448) is the reading taken.  amax is exact in double; the scale
+ * is one IEEE fp32 division.
+ */
+float orc_amax_scale_bf16(const uint16_t *xbits, int64_t n)
+{
+    int64_t i;
+    double amax = 0.0;
+    volatile float a, q;
+    for (i = 0; i < n; ++i) {
+        double x = (double)bf16_bits_to_float(xbits[i]);
+        if (isfinite(x) && fabs(x) > amax)
+            amax = fabs(x);
+    }
+    if (amax == 0.0)
+        return 1.0f;
+    a = (float)amax;
+    q = a / 448.0f;
+    return q;
+}
+
 /* ------------------------------------------------------------------------- */
 /* pool indexing (the documented layout)                                      */
 /* ------------------------------------------------------------------------- */
