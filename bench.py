@@ -9,6 +9,7 @@ identical values for comparison.  Prints ONE JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload b32_8k]
   python bench.py --impl reference ...     # the CPU oracle, timed on host cores
+  python bench.py --capacity [--kv-budget-gib 4]   # admission curve, BF16 vs FP8 cache
 
 Multi-GPU (torchrun): every rank runs an independent replica (its own requests
 and pool); nothing on the data path is exchanged, only the timing is reduced.
@@ -452,6 +453,94 @@ def time_e2e(pool, steps: int, warmup: int):
     return ms, h2d, d2h
 
 
+def run_capacity(args, rank, world):
+    """Admission at a fixed KV budget (one layer): how many 8192-token requests of
+    the b32_8k shape (Hq=64, Hkv=8, D=128, page 16) fit in the pool with a BF16
+    cache and with an e4m3 cache, and decode-attention tokens/s and GB/s at
+    concurrencies up to each cap.  Cache values are random codes: only timing is
+    taken here (the same kernels are parity-tested elsewhere).  L2 is flushed
+    before every timed launch."""
+    import fp8_paged_kv_gb300 as fpk
+    from fp8_paged_kv_gb300 import build as fbuild
+    if rank == 0 or world == 1:
+        fbuild.build()
+    barrier(world)
+    fpk.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    Hq, Hkv, D, ps, L = 64, 8, 128, 16, 8192
+    budget = int(args.kv_budget_gib * 2**30)
+    ppr = L // ps
+    g = torch.Generator(device=dev)
+    g.manual_seed(7 + rank)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev)
+    curves = {}
+    with ClockSampler(local_rank()) as clk:
+        for fp8 in (False, True):
+            b = 1 if fp8 else 2
+            page_bytes = 2 * Hkv * ps * D * b
+            num_pages = budget // page_bytes
+            cap = num_pages // ppr
+            n = num_pages * page_bytes // b
+            if fp8:
+                pool = torch.randint(0, 0x7F, (n,), dtype=torch.uint8, device=dev, generator=g)
+                pool |= torch.randint(0, 2, (n,), dtype=torch.uint8, device=dev, generator=g) << 7
+            else:
+                pool = torch.randn(n, device=dev, generator=g, dtype=torch.float32).to(torch.bfloat16)
+            perm = torch.randperm(num_pages, device=dev, generator=g).to(torch.int32)
+            conc = sorted({c for c in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024) if c <= cap} | {cap})
+            pts = []
+            for c in conc:
+                pt = perm[:c * ppr].view(c, ppr).contiguous()
+                lens = torch.full((c,), L, dtype=torch.int32, device=dev)
+                q = torch.randn(c, Hq, D, device=dev, generator=g).to(torch.bfloat16)
+                out = torch.empty(c, Hq, D, device=dev)
+                lse = torch.empty(c, Hq, device=dev)
+                ws = torch.zeros(fpk.fpk_decode_workspace_bytes(c, Hq, Hkv, D, 0), dtype=torch.uint8,
+                                 device=dev)
+                ks = torch.tensor([0.01], device=dev)
+                kw = dict(Hkv=Hkv, page_size=ps, num_pages=num_pages, sm_scale=D ** -0.5)
+
+                def run():
+                    if fp8:
+                        fpk.fpk_paged_decode_attn_fp8(q, pool, ks, ks, pt, lens, None, out, lse, ws, **kw)
+                    else:
+                        fpk.fpk_paged_decode_attn_bf16(q, pool, pt, lens, None, out, lse, ws, **kw)
+                t = []
+                for i in range(3 + args.capacity_reps):
+                    flush.zero_()
+                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    run()
+                    e.record(s)
+                    torch.cuda.synchronize(dev)
+                    if i >= 3:
+                        t.append(a.elapsed_time(e))
+                ms = statistics.median(t)
+                kv = c * L * 2 * Hkv * D * b
+                pts.append({"requests": c, "attn_us": ms * 1e3, "tokens_per_s": c / (ms * 1e-3),
+                            "gbs": (kv + c * ppr * 4 + c * Hq * D * 2 + c * Hq * (D + 1) * 4) / (ms * 1e-3) / 1e9})
+                del ws, q, out, lse
+            curves["fp8" if fp8 else "bf16"] = {"cap_requests": cap, "pool_pages": num_pages,
+                                                "points": pts}
+            del pool, perm
+            torch.cuda.empty_cache()
+    bf, f8 = curves["bf16"], curves["fp8"]
+    line = {"mode": "capacity", "kv_budget_gib": args.kv_budget_gib, "context": L,
+            "shape": f"Hq={Hq}, Hkv={Hkv}, D={D}, page_size={ps}, one layer",
+            "bf16": bf, "fp8": f8,
+            "fp8_over_bf16_cap": f8["cap_requests"] / max(1, bf["cap_requests"]),
+            "fp8_at_cap_over_bf16_at_cap_tokens_per_s":
+                f8["points"][-1]["tokens_per_s"] / bf["points"][-1]["tokens_per_s"],
+            "l2": "flushed (512 MB write) before every timed launch", "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def local_rank() -> int:
+    return int(os.environ.get("LOCAL_RANK", "0"))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -461,12 +550,19 @@ def main():
     ap.add_argument("--workload", default="b32_8k")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--capacity", action="store_true",
+                    help="admission curve at a fixed KV budget instead of the step benchmark")
+    ap.add_argument("--kv-budget-gib", type=float, default=4.0)
+    ap.add_argument("--capacity-reps", type=int, default=10)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.capacity:
+        run_capacity(args, rank, world)
         return
 
     import fp8_paged_kv_gb300 as fpk

@@ -936,6 +936,15 @@ WsLayout layout(int64_t B, int64_t Hkv, int64_t G, int64_t W) {
   return l;
 }
 
+// The automatic split count: one wave of CTAs, but no more than 16 splits per
+// (request, kv head) segment -- small batches then keep the one-level combine
+// and CTAs with enough tiles to cover their start-up.
+constexpr int kAutoSplitsPerSegment = 16;
+int auto_splits(int wave, int B, int Hkv) {
+  const int64_t cap = static_cast<int64_t>(kAutoSplitsPerSegment) * B * Hkv;
+  return cap < wave ? static_cast<int>(cap) : wave;
+}
+
 int auto_workers(int dev) {
   const int sms = device_sm_count(dev);
   const int a8 = prepare_kernel<true>(dev);
@@ -975,7 +984,7 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
   const int per_sm = prepare_kernel<kFp8>(dev);
   const int wave = device_sm_count(dev) * per_sm;  // CTAs resident at once
   if (per_sm <= 0 || wave <= 0) return FPK_ECUDA;
-  const int W = num_splits == 0 ? wave : num_splits;
+  const int W = num_splits == 0 ? auto_splits(wave, B, Hkv) : num_splits;
   const int ctas = W < wave ? W : wave;  // more splits than that: a CTA runs several in turn
   const int G = Hq / Hkv;
   const WsLayout l = layout(B, Hkv, G, W);
@@ -1123,7 +1132,7 @@ extern "C" int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k
   if (W == 0) {
     const int per_sm = fpk::prepare_kernel<true>(dev);
     if (per_sm <= 0) return FPK_ECUDA;
-    W = fpk::device_sm_count(dev) * per_sm;
+    W = fpk::auto_splits(fpk::device_sm_count(dev) * per_sm, B, Hkv);
     if (W <= 0) return FPK_ECUDA;
   }
   const fpk::WsLayout l = fpk::layout(B, Hkv, Hq / Hkv, W);

@@ -264,7 +264,8 @@ size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  *   num_splits: number of split-KV work units the batch's KV tiles are
  *               divided into (balanced by tile count across all requests and
  *               kv heads); each split's partial enters the log-sum-exp
- *               combine.  0 = automatic (one wave of CTAs).  With equal
+ *               combine.  0 = automatic: one wave of CTAs, at most 16 per
+ *               (request, kv head).  With equal
  *               context lengths, num_splits = S * B * Hkv gives exactly S
  *               splits per (request, kv head).  At most one wave of CTAs is
  *               launched; beyond that a CTA runs several splits in turn.
