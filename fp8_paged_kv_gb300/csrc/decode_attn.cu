@@ -93,6 +93,7 @@ struct AttnArgs {
   float2* part_ml;
   float* part_o;
   int B, Hq, Hkv, G, page_size, num_pages, max_pages, W;
+  int auto_split;  // W is the automatic count: the kernel may pick one split per segment
   float sm_scale_log2;
 };
 
@@ -127,10 +128,10 @@ __device__ __forceinline__ int worker_of(int64_t x, int64_t T, int W) {
 
 // The next piece of a CTA's tile range: the longest run that stays inside one
 // (request, kv head) segment and one split.
-__device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, int64_t T, Piece& p) {
+__device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, int64_t T, int W, Piece& p) {
   if (c.remaining <= 0) return false;
-  const int s = worker_of(c.x, T, a.W);
-  const int64_t split_end = (static_cast<int64_t>(s) + 1) * T / a.W;
+  const int s = worker_of(c.x, T, W);
+  const int64_t split_end = (static_cast<int64_t>(s) + 1) * T / W;
   int64_t take64 = c.n - c.t;
   if (c.remaining < take64) take64 = c.remaining;
   if (split_end - c.x < take64) take64 = split_end - c.x;
@@ -186,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   int* s_stage_fault = reinterpret_cast<int*>(bars + 2 * C::kStages + 3);
 
   __shared__ int64_t s_warp_sum[kThreads / 32];
+  __shared__ int s_warp_nz[kThreads / 32], s_warp_min[kThreads / 32], s_warp_max[kThreads / 32];
   __shared__ int s_start[4];
   __shared__ int s_last;
 
@@ -200,32 +202,62 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   const int rb = tid * chunk;
   const int re = min(a.B, rb + chunk);
   int64_t mine = 0;
-  for (int r = rb; r < re; ++r) mine += tiles_of(a, r);
+  int nz = 0, tmin = 0x7fffffff, tmax = 0;  // requests with tiles; their fewest and most
+  for (int r = rb; r < re; ++r) {
+    const int n = tiles_of(a, r);
+    mine += n;
+    if (n > 0) {
+      ++nz;
+      tmin = min(tmin, n);
+      tmax = max(tmax, n);
+    }
+  }
   int64_t incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int64_t v = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += v;
   }
+  nz = __reduce_add_sync(kFull, nz);
+  tmin = __reduce_min_sync(kFull, tmin);
+  tmax = __reduce_max_sync(kFull, tmax);
   if (lane == 31) s_warp_sum[warp] = incl;
+  if (lane == 0) {
+    s_warp_nz[warp] = nz;
+    s_warp_min[warp] = tmin;
+    s_warp_max[warp] = tmax;
+  }
   if (tid == 0) {
     s_start[0] = -1;
   }
   __syncthreads();
   int64_t before = 0, total = 0;
+  int nz_all = 0, tmin_all = 0x7fffffff, tmax_all = 0;
 #pragma unroll
   for (int i = 0; i < kThreads / 32; ++i) {
     if (i < warp) before += s_warp_sum[i];
     total += s_warp_sum[i];
+    nz_all += s_warp_nz[i];
+    tmin_all = min(tmin_all, s_warp_min[i]);
+    tmax_all = max(tmax_all, s_warp_max[i]);
   }
   const int64_t excl = before + incl - mine;
   const int64_t T = total * a.Hkv;
-  // this CTA runs splits [s0, s1) one after another: tiles [b0, b1)
   const int nctas = static_cast<int>(gridDim.x);
-  const int64_t s0 = static_cast<int64_t>(w) * a.W / nctas;
-  const int64_t s1 = static_cast<int64_t>(w + 1) * a.W / nctas;
-  const int64_t b0 = s0 * T / a.W;
-  const int64_t b1 = s1 * T / a.W;
+  // Split count.  With the automatic count, a batch whose (request, kv head)
+  // segments all have the same length and number between 3/4 of the CTAs and
+  // all of them runs one whole segment per CTA: no split partials, no
+  // cross-CTA combine (it costs less than the idle quarter of the CTAs).
+  int W = a.W;
+  if (a.auto_split && nz_all > 0 && tmin_all == tmax_all) {
+    const int64_t segs = static_cast<int64_t>(nz_all) * a.Hkv;
+    if (4 * segs >= 3 * static_cast<int64_t>(nctas) && segs <= nctas) W = static_cast<int>(segs);
+  }
+  // this CTA runs splits [s0, s1) one after another: tiles [b0, b1)
+  const int64_t s0 = static_cast<int64_t>(w) * W / nctas;
+  const int64_t s1 = static_cast<int64_t>(w + 1) * W / nctas;
+  const int64_t b0 = s0 * T / W;
+  const int64_t b1 = s1 * T / W;
   // requests that read nothing (empty, aborted, over-long) get out = 0 and
   // lse = -inf; the CTAs share this round-robin
   for (int r = w; r < a.B; r += nctas) {
@@ -302,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     Piece p;
     uint32_t j = 0;  // stages issued so far
     bool ok = true;
-    while (ok && next_piece(cur, a, T, p)) {
+    while (ok && next_piece(cur, a, T, W, p)) {
       const int32_t* ptrow = a.page_table + static_cast<int64_t>(p.r) * a.max_pages;
       const int nst = (p.t1 - p.t0 + 1) >> 1;
       auto load_id = [&](int k0) {
@@ -435,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   auto combine = [&](const Members& mb, int n, int r, int h, int64_t dst) -> bool {
     auto slot_of = [&](int k) -> int64_t {
       const int i = mb.i0 + k * mb.stride;
-      return mb.seg + (mb.dense ? mb.w0 + i : worker_of(mb.xseg + i, T, a.W));
+      return mb.seg + (mb.dense ? mb.w0 + i : worker_of(mb.xseg + i, T, W));
     };
     float2* s_w = reinterpret_cast<float2*>(s_o);
     constexpr int kChunk = kConsumerWarps * kGroupMax * kMergeStride / (2 * kGroupMax);
@@ -543,11 +575,11 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   auto publish_partial = [&](const Piece& p, int seg) -> bool {
     constexpr int kDirect = 16;
     const int64_t xseg = p.x0 - p.t0;  // global index of the segment's first tile
-    const int w0 = worker_of(xseg, T, a.W);
-    const int w1 = worker_of(xseg + p.n - 1, T, a.W);
+    const int w0 = worker_of(xseg, T, W);
+    const int w1 = worker_of(xseg + p.n - 1, T, W);
     // splits holding a piece of this segment: all of w0..w1 when every split
     // owns tiles (T >= W), else one per tile (the i-th is the owner of tile i)
-    const bool dense = T >= a.W;
+    const bool dense = T >= W;
     const int nsl = dense ? w1 - w0 + 1 : p.n;
     const int me = dense ? p.s - w0 : p.t0;
     Members mb;
@@ -568,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       const int gi = me / K;
       mb.i0 = gi * K;
       n = min(K, nsl - mb.i0);
-      dst = seg + (dense ? w0 + mb.i0 : worker_of(xseg + mb.i0, T, a.W));
+      dst = seg + (dense ? w0 + mb.i0 : worker_of(xseg + mb.i0, T, W));
       ctr = a.group_count + dst;
     }
     for (;;) {
@@ -588,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     }
   };
 
-  while (ok && next_piece(cur, a, T, p)) {
+  while (ok && next_piece(cur, a, T, W, p)) {
     const int ntiles = p.t1 - p.t0;
     const int L = __ldg(a.seq_lens + p.r);
     // ---- query fragments (B operand of S^T = K Q^T), heads of this kv group
@@ -1013,6 +1045,7 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
   a.num_pages = num_pages;
   a.max_pages = max_pages;
   a.W = W;
+  a.auto_split = num_splits == 0;
   a.sm_scale_log2 = sm_scale * kLog2e;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   paged_decode_split_kernel<kFp8><<<ctas, kThreads, Cfg<kFp8>::kSmemBytes, s>>>(a);
@@ -1141,6 +1174,6 @@ extern "C" int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k
   if (cudaMemsetAsync(scratch, 0, l.part_ml, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FPK_ECUDA;
   return fpk::attn_entry<true>(q, kv_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
-                               abort_mask, out, lse, scratch, fpk::kNoAllocScratchBytes, W, sm_scale,
+                               abort_mask, out, lse, scratch, fpk::kNoAllocScratchBytes, num_splits, sm_scale,
                                B, Hq, Hkv, D, page_size, num_pages, stream);
 }

@@ -69,6 +69,21 @@ def test_split_counts(fp8, num_splits):
     assert_attention_close(out, lse, ro, rl, f"splits={num_splits}")
 
 
+@pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("abort_one", [False, True])
+def test_uniform_batch_one_segment_per_cta(fp8, abort_one):
+    # 30 requests x 8 kv heads of equal length: with the automatic split count
+    # (a wave of 304 CTAs on GB300) every CTA takes one whole segment
+    lens = [200] * 30
+    wl = custom(83, B=30, Hq=16, Hkv=8, ps=16, prompt_lens=lens, steps=0)
+    abort = None
+    if abort_one:
+        abort = np.zeros(wl.B, np.uint8)
+        abort[7] = 1
+    out, lse, ro, rl = _run_case(wl, fp8, 0, abort=abort, use_mask=abort_one)
+    assert_attention_close(out, lse, ro, rl, f"uniform fp8={fp8} abort={abort_one}")
+
+
 def test_split_invariance():
     lens = [3000, 1, 900]
     wl = custom(80, B=3, Hq=32, Hkv=4, ps=32, prompt_lens=lens, steps=0)
