@@ -59,6 +59,11 @@ SIGNATURES = {
     "fpk_paged_decode_attn_fp8_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P,
                                                          _P, _I32, _F, _I32, _I32, _I32, _I32, _I32,
                                                          _I32, _P]),
+    "fpk_decode_step_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P,
+                                           _P, _P, _SZ, _I32, _F, _I32, _I32, _I32, _I32, _I32,
+                                           _I32, _P]),
+    "fpk_decode_step_bf16": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                            _SZ, _I32, _F, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "fpk_decode_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
 }
 
@@ -254,6 +259,36 @@ def fpk_paged_decode_attn_fp8(q, kv_pool, k_scale, v_scale, page_table, seq_lens
         _ptr(lse, _F32, "lse", True), _ptr(workspace, _U8, "workspace"),
         workspace.numel(), num_splits, sm_scale, B, Hq, Hkv, D, page_size, num_pages,
         _stream(stream)), "fpk_paged_decode_attn_fp8")
+
+
+def fpk_decode_step_fp8(k_new, v_new, kv_pool, k_scale, v_scale, page_table, seq_lens, live_tags,
+                        expected_tags, abort_mask, q, out, lse, workspace, *, Hkv, page_size,
+                        num_pages, sm_scale, num_splits=0, stream=None):
+    B, Hq, D = q.shape
+    _check(load_library().fpk_decode_step_fp8(
+        _ptr(k_new, _BF16_LIKE, "k_new"), _ptr(v_new, _BF16_LIKE, "v_new"), _ptr(kv_pool, _U8, "kv_pool"),
+        _ptr(k_scale, _F32, "k_scale"), _ptr(v_scale, _F32, "v_scale"),
+        _ptr(page_table, _I32T, "page_table"), page_table.shape[1], _ptr(seq_lens, _I32T, "seq_lens"),
+        _ptr(live_tags, _TAGS, "live_tags", True), _ptr(expected_tags, _TAGS, "expected_tags", True),
+        _ptr(abort_mask, _U8, "abort_mask", True), _ptr(q, _BF16_LIKE, "q"), _ptr(out, _F32, "out"),
+        _ptr(lse, _F32, "lse", True), _ptr(workspace, _U8, "workspace"), workspace.numel(),
+        num_splits, sm_scale, B, Hq, Hkv, D, page_size, num_pages, _stream(stream)),
+        "fpk_decode_step_fp8")
+
+
+def fpk_decode_step_bf16(k_new, v_new, kv_pool, page_table, seq_lens, live_tags, expected_tags,
+                         abort_mask, q, out, lse, workspace, *, Hkv, page_size, num_pages, sm_scale,
+                         num_splits=0, stream=None):
+    B, Hq, D = q.shape
+    _check(load_library().fpk_decode_step_bf16(
+        _ptr(k_new, _BF16_LIKE, "k_new"), _ptr(v_new, _BF16_LIKE, "v_new"),
+        _ptr(kv_pool, _BF16_LIKE, "kv_pool"), _ptr(page_table, _I32T, "page_table"),
+        page_table.shape[1], _ptr(seq_lens, _I32T, "seq_lens"),
+        _ptr(live_tags, _TAGS, "live_tags", True), _ptr(expected_tags, _TAGS, "expected_tags", True),
+        _ptr(abort_mask, _U8, "abort_mask", True), _ptr(q, _BF16_LIKE, "q"), _ptr(out, _F32, "out"),
+        _ptr(lse, _F32, "lse", True),
+        _ptr(workspace, _U8, "workspace"), workspace.numel(), num_splits, sm_scale, B, Hq, Hkv, D,
+        page_size, num_pages, _stream(stream)), "fpk_decode_step_bf16")
 
 
 def fpk_paged_decode_attn_bf16(q, kv_pool, page_table, seq_lens, abort_mask, out, lse,

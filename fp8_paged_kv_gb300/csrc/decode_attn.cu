@@ -40,6 +40,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "step_ops.cuh"
 
 namespace fpk {
 namespace {
@@ -116,8 +117,16 @@ struct Cursor {
   int64_t x, remaining;
 };
 
+// Tiles of request r in the work list: its context length only.  The work
+// list is built before the abort mask may be read (the mask can come from the
+// kernel launched just before this one); pieces of aborted requests are
+// skipped after the dependency wait (is_aborted).
 __device__ __forceinline__ int tiles_of(const AttnArgs& a, int r) {
-  return tiles_of_request(a.seq_lens, a.abort_mask, r, a.max_pages, a.page_size);
+  return tiles_of_request(a.seq_lens, nullptr, r, a.max_pages, a.page_size);
+}
+
+__device__ __forceinline__ bool is_aborted(const AttnArgs& a, int r) {
+  return a.abort_mask != nullptr && __ldcg(a.abort_mask + r) != 0;
 }
 
 // Worker w owns global tiles [floor(w T / W), floor((w+1) T / W)); the owner
@@ -258,18 +267,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   const int64_t s1 = static_cast<int64_t>(w + 1) * W / nctas;
   const int64_t b0 = s0 * T / W;
   const int64_t b1 = s1 * T / W;
-  // requests that read nothing (empty, aborted, over-long) get out = 0 and
-  // lse = -inf; the CTAs share this round-robin
-  for (int r = w; r < a.B; r += nctas) {
-    if (tiles_of(a, r) == 0) {
-      float* orow = a.out + static_cast<int64_t>(r) * a.Hq * kDim;
-      for (int i = tid; i < a.Hq * kDim; i += kThreads) orow[i] = 0.f;
-      if (a.lse != nullptr)
-        for (int i = tid; i < a.Hq; i += kThreads) a.lse[static_cast<int64_t>(r) * a.Hq + i] = -INFINITY;
-    }
-  }
-  if (b0 >= b1) return;  // uniform over the CTA: empty range
-  if (mine > 0 && b0 >= excl * a.Hkv && b0 < (excl + mine) * a.Hkv) {
+  const bool has_work = b0 < b1;  // uniform over the CTA
+  if (has_work && mine > 0 && b0 >= excl * a.Hkv && b0 < (excl + mine) * a.Hkv) {
     int64_t base = excl * a.Hkv;
     for (int r = rb; r < re; ++r) {
       const int n = tiles_of(a, r);
@@ -302,6 +301,27 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     fence_barrier_init();
   }
   __syncthreads();
+  // Everything above reads only inputs the caller supplied before the
+  // previous kernel on the stream began; from here on the abort mask and the
+  // cache may be read (a no-op unless launched as a programmatic dependent).
+  griddep_wait();
+  // requests that read nothing (empty, aborted, over-long) get out = 0 and
+  // lse = -inf; the CTAs share this round-robin (in a working CTA the
+  // consumer warps do it while the producer starts its copies)
+  auto zero_dead_rows = [&](int t0, int nt) {
+    for (int r = w; r < a.B; r += nctas) {
+      if (tiles_of(a, r) == 0 || is_aborted(a, r)) {
+        float* orow = a.out + static_cast<int64_t>(r) * a.Hq * kDim;
+        for (int i = t0; i < a.Hq * kDim; i += nt) orow[i] = 0.f;
+        if (a.lse != nullptr)
+          for (int i = t0; i < a.Hq; i += nt) a.lse[static_cast<int64_t>(r) * a.Hq + i] = -INFINITY;
+      }
+    }
+  };
+  if (!has_work) {
+    zero_dead_rows(tid, kThreads);
+    return;
+  }
   if (s_start[0] < 0) {  // inconsistent inputs (cannot happen): nothing to do
     if (tid == 0) atomicOr(a.status, kStatusBadStart);
     return;
@@ -334,6 +354,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     Piece p;
     uint32_t j = 0;  // stages issued so far
     bool ok = true;
+    int ab_r = -1;      // request whose abort flag is cached
+    bool ab = false;
     while (ok && next_piece(cur, a, T, W, p)) {
       const int32_t* ptrow = a.page_table + static_cast<int64_t>(p.r) * a.max_pages;
       const int nst = (p.t1 - p.t0 + 1) >> 1;
@@ -345,7 +367,12 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         }
         return pg;
       };
-      int pg = load_id(0);
+      int pg = load_id(0);  // table reads only: harmless for an aborted request
+      if (p.r != ab_r) {
+        ab_r = p.r;
+        ab = is_aborted(a, p.r);
+      }
+      if (ab) continue;  // the consumers skip it too
       for (int k0 = 0; k0 < nst && ok; k0 += kBatch) {
         const int cnt = min(kBatch, nst - k0);
         const int nxt = load_id(k0 + kBatch);  // prefetch (unused past the piece)
@@ -620,7 +647,14 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     }
   };
 
+  zero_dead_rows(ct_all, kConsumerWarps * 32);
+  int ab_r = -1;  // request whose abort flag is cached
+  bool ab = false;
   while (ok && next_piece(cur, a, T, W, p)) {
+    if (p.r != ab_r) {
+      ab_r = p.r;
+      ab = is_aborted(a, p.r);  // used after the query loads below are issued
+    }
     const int ntiles = p.t1 - p.t0;
     const int L = __ldg(a.seq_lens + p.r);
     // ---- query fragments (B operand of S^T = K Q^T), heads of this kv group
@@ -674,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         mult_own = has ? a.sm_scale_log2 : 0.f;
       }
     }
+    if (ab) continue;  // output zeroed above; nothing read
     // score multipliers of the two heads (2*t4, 2*t4+1) whose columns this lane holds
     const float mult0 = __shfl_sync(kFull, mult_own, 8 * t4);
     const float mult1 = __shfl_sync(kFull, mult_own, 8 * t4 + 4);
@@ -996,13 +1031,15 @@ int check_attn_shapes(int B, int Hq, int Hkv, int D, int page_size, int num_page
   return FPK_OK;
 }
 
+enum class AttnLaunch { kPlain, kCheckOnly, kAfterStepWrite };
+
 template <bool kFp8>
 int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
                const float* v_scale, const int32_t* page_table, int32_t max_pages,
                const int32_t* seq_lens, const uint8_t* abort_mask, float* out, float* lse,
                void* workspace, size_t workspace_bytes, int32_t num_splits, float sm_scale,
                int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
-               int32_t num_pages, void* stream) {
+               int32_t num_pages, void* stream, AttnLaunch mode = AttnLaunch::kPlain) {
   int st = check_attn_shapes(B, Hq, Hkv, D, page_size, num_pages, max_pages, num_splits);
   if (st != FPK_OK) return st;
   if (B == 0) return FPK_OK;
@@ -1047,8 +1084,26 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
   a.W = W;
   a.auto_split = num_splits == 0;
   a.sm_scale_log2 = sm_scale * kLog2e;
+  if (mode == AttnLaunch::kCheckOnly) return FPK_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  paged_decode_split_kernel<kFp8><<<ctas, kThreads, Cfg<kFp8>::kSmemBytes, s>>>(a);
+  if (mode == AttnLaunch::kPlain) {
+    paged_decode_split_kernel<kFp8><<<ctas, kThreads, Cfg<kFp8>::kSmemBytes, s>>>(a);
+    return checked_launch_status();
+  }
+  // launched as a programmatic dependent of the step's write + check kernel:
+  // its set-up overlaps that kernel; it reads the mask and the cache only
+  // after griddep_wait()
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<kFp8>::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<kFp8>, a) != cudaSuccess) return FPK_ECUDA;
   return checked_launch_status();
 }
 
@@ -1093,6 +1148,60 @@ extern "C" int fpk_paged_decode_attn_bf16(const void* q, const void* kv_pool,
   return fpk::attn_entry<false>(q, kv_pool, nullptr, nullptr, page_table, max_pages, seq_lens,
                                 abort_mask, out, lse, workspace, workspace_bytes, num_splits,
                                 sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream);
+}
+
+extern "C" int fpk_decode_step_fp8(const void* k_new, const void* v_new, uint8_t* kv_pool,
+                                   const float* k_scale, const float* v_scale,
+                                   const int32_t* page_table, int32_t max_pages,
+                                   const int32_t* seq_lens, const uint32_t* live_tags,
+                                   const uint32_t* expected_tags, uint8_t* abort_mask, const void* q,
+                                   float* out, float* lse, void* workspace, size_t workspace_bytes,
+                                   int32_t num_splits, float sm_scale, int32_t B, int32_t Hq,
+                                   int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                                   void* stream) {
+  // every argument of both launches is checked before either is issued
+  int st = fpk::attn_entry<true>(q, kv_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
+                                 abort_mask, out, lse, workspace, workspace_bytes, num_splits,
+                                 sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream,
+                                 fpk::AttnLaunch::kCheckOnly);
+  if (st != FPK_OK) return st;
+  if ((live_tags != nullptr || expected_tags != nullptr) && (!live_tags || !expected_tags || !abort_mask))
+    return FPK_EINVAL;
+  if (live_tags == nullptr) abort_mask = nullptr;  // the no-op tracker: no check, no mask
+  st = fpk::append_check_entry(true, k_new, v_new, kv_pool, k_scale, v_scale, page_table, max_pages,
+                               seq_lens, live_tags, expected_tags, abort_mask, B, Hkv, D, page_size,
+                               num_pages, stream);
+  if (st != FPK_OK) return st;
+  return fpk::attn_entry<true>(q, kv_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
+                               abort_mask, out, lse, workspace, workspace_bytes, num_splits,
+                               sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream,
+                               fpk::AttnLaunch::kAfterStepWrite);
+}
+
+extern "C" int fpk_decode_step_bf16(const void* k_new, const void* v_new, void* kv_pool,
+                                    const int32_t* page_table, int32_t max_pages,
+                                    const int32_t* seq_lens, const uint32_t* live_tags,
+                                    const uint32_t* expected_tags, uint8_t* abort_mask, const void* q,
+                                    float* out, float* lse, void* workspace, size_t workspace_bytes,
+                                    int32_t num_splits, float sm_scale, int32_t B, int32_t Hq,
+                                    int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                                    void* stream) {
+  int st = fpk::attn_entry<false>(q, kv_pool, nullptr, nullptr, page_table, max_pages, seq_lens,
+                                  abort_mask, out, lse, workspace, workspace_bytes, num_splits,
+                                  sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream,
+                                  fpk::AttnLaunch::kCheckOnly);
+  if (st != FPK_OK) return st;
+  if ((live_tags != nullptr || expected_tags != nullptr) && (!live_tags || !expected_tags || !abort_mask))
+    return FPK_EINVAL;
+  if (live_tags == nullptr) abort_mask = nullptr;  // the no-op tracker: no check, no mask
+  st = fpk::append_check_entry(false, k_new, v_new, kv_pool, nullptr, nullptr, page_table, max_pages,
+                               seq_lens, live_tags, expected_tags, abort_mask, B, Hkv, D, page_size,
+                               num_pages, stream);
+  if (st != FPK_OK) return st;
+  return fpk::attn_entry<false>(q, kv_pool, nullptr, nullptr, page_table, max_pages, seq_lens,
+                                abort_mask, out, lse, workspace, workspace_bytes, num_splits,
+                                sm_scale, B, Hq, Hkv, D, page_size, num_pages, stream,
+                               fpk::AttnLaunch::kAfterStepWrite);
 }
 
 extern "C" int fpk_decode_status(const void* workspace, int32_t* status, void* stream) {

@@ -24,7 +24,12 @@ __global__ void __launch_bounds__(kValidateThreads) append_check_kernel(WriteArg
                                                                         const uint32_t* live_tags,
                                                                         const uint32_t* expected_tags,
                                                                         uint8_t* abort_mask) {
-  if (blockIdx.x < static_cast<unsigned>(w.B)) {
+  // a programmatically dependent attention launch may start its set-up now;
+  // it reads nothing this kernel writes before this grid has completed
+  griddep_launch_dependents();
+  // no tags: the no-op tracker -- no check CTAs, unguarded writes
+  const int nchk = (live_tags != nullptr && expected_tags != nullptr) ? w.B : 0;
+  if (static_cast<int>(blockIdx.x) < nchk) {
     check_request(w.page_table, expected_tags, w.seq_lens, w.max_pages, live_tags, w.num_pages,
                   w.page_size, abort_mask, blockIdx.x);
     return;
@@ -32,11 +37,13 @@ __global__ void __launch_bounds__(kValidateThreads) append_check_kernel(WriteArg
   const int64_t units = w.rows * w.Hkv * (w.D >> 3);
   const float ks = kFp8 ? __ldg(w.k_scale) : 1.f;
   const float vs = kFp8 ? __ldg(w.v_scale) : 1.f;
-  const int64_t stride = static_cast<int64_t>(gridDim.x - w.B) * blockDim.x;
-  for (int64_t u = static_cast<int64_t>(blockIdx.x - w.B) * blockDim.x + threadIdx.x; u < units;
+  const int64_t stride = static_cast<int64_t>(gridDim.x - nchk) * blockDim.x;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x - nchk) * blockDim.x + threadIdx.x; u < units;
        u += stride)
     write_unit<kFp8, false>(w, u, ks, vs);
 }
+
+}  // namespace
 
 int append_check_entry(bool fp8, const void* k_new, const void* v_new, void* kv_pool,
                        const float* k_scale, const float* v_scale, const int32_t* page_table,
@@ -47,9 +54,11 @@ int append_check_entry(bool fp8, const void* k_new, const void* v_new, void* kv_
     return FPK_EINVAL;
   if (D != 128 || page_size % 16 != 0 || page_size > 256) return FPK_EUNSUPPORTED;
   if (B == 0) return FPK_OK;
-  if (!k_new || !v_new || !kv_pool || !page_table || !seq_lens || !live_tags || !expected_tags ||
-      !abort_mask)
-    return FPK_EINVAL;
+  if (!k_new || !v_new || !kv_pool || !page_table || !seq_lens) return FPK_EINVAL;
+  // the check needs both tag arrays and the mask; with neither tag array it is
+  // the no-op tracker
+  const bool check = live_tags != nullptr || expected_tags != nullptr;
+  if (check && (!live_tags || !expected_tags || !abort_mask)) return FPK_EINVAL;
   if (fp8 && (!k_scale || !v_scale)) return FPK_EINVAL;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(kv_pool)) return FPK_EINVAL;
   WriteArgs w;
@@ -61,9 +70,9 @@ int append_check_entry(bool fp8, const void* k_new, const void* v_new, void* kv_
   w.k_scale = k_scale;
   w.v_scale = v_scale;
   w.page_table = page_table;
-  w.live_tags = live_tags;
-  w.expected_tags = expected_tags;
-  w.abort_mask = abort_mask;
+  w.live_tags = check ? live_tags : nullptr;
+  w.expected_tags = check ? expected_tags : nullptr;
+  w.abort_mask = check ? abort_mask : nullptr;
   w.rows = B;
   w.B = B;
   w.Hkv = Hkv;
@@ -73,14 +82,13 @@ int append_check_entry(bool fp8, const void* k_new, const void* v_new, void* kv_
   w.max_pages = max_pages;
   const int64_t units = static_cast<int64_t>(B) * Hkv * (D >> 3);
   const int64_t want = (units + kValidateThreads - 1) / kValidateThreads;
-  const int grid = B + static_cast<int>(want < kWriteCtas ? want : kWriteCtas);
+  const int grid = (check ? B : 0) + static_cast<int>(want < kWriteCtas ? want : kWriteCtas);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (fp8) append_check_kernel<true><<<grid, kValidateThreads, 0, s>>>(w, live_tags, expected_tags, abort_mask);
-  else append_check_kernel<false><<<grid, kValidateThreads, 0, s>>>(w, live_tags, expected_tags, abort_mask);
+  if (fp8) append_check_kernel<true><<<grid, kValidateThreads, 0, s>>>(w, w.live_tags, w.expected_tags, w.abort_mask);
+  else append_check_kernel<false><<<grid, kValidateThreads, 0, s>>>(w, w.live_tags, w.expected_tags, w.abort_mask);
   return checked_launch_status();
 }
 
-}  // namespace
 }  // namespace fpk
 
 extern "C" int fpk_decode_append_check_fp8(const void* k_new, const void* v_new, uint8_t* kv_pool,

@@ -105,9 +105,12 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, int64_t u, float 
   }
 }
 
-// One CTA per request.  Each thread checks up to 4 table entries per round
-// with all loads of the round issued before any compare.
+// One CTA per request.  Each thread checks up to kCheckPerThread table
+// entries per round: all table loads of the round, then all live-tag gathers
+// (at a clamped, always valid index, so none waits behind a compare), then
+// the compares -- two dependent memory round trips per round.
 constexpr int kValidateThreads = 256;
+constexpr int kCheckPerThread = 8;
 
 // The check of request r by one whole CTA of kValidateThreads threads: writes
 // abort_mask[r] and returns whether the request aborts (to every thread).
@@ -116,33 +119,57 @@ __device__ __forceinline__ int check_request(const int32_t* __restrict__ page_ta
                                              const int32_t* __restrict__ seq_lens, int max_pages,
                                              const uint32_t* __restrict__ live_tags, int num_pages,
                                              int page_size, uint8_t* __restrict__ abort_mask, int r) {
-  const int L = __ldg(seq_lens + r);
-  const int P = L > 0 ? (L + page_size - 1) / page_size : 0;
-  int bad = P > max_pages;
   const int32_t* pt = page_table + static_cast<int64_t>(r) * max_pages;
   const uint32_t* ex = expected_tags + static_cast<int64_t>(r) * max_pages;
-  for (int base = 0; base < P && !bad; base += 4 * kValidateThreads) {
-    int page[4];
-    uint32_t want[4];
+  // The first round's table loads do not wait for the context length: they
+  // cover the row's first entries (up to its width), and only entries below
+  // the request's page count are compared.
+  const int L = __ldg(seq_lens + r);
+  int P = -1;  // known once L has arrived
+  int bad = 0;
+  for (int base = 0; base < max_pages && (P < 0 || (base < P && !bad));
+       base += kCheckPerThread * kValidateThreads) {
+    int page[kCheckPerThread];
+    uint32_t want[kCheckPerThread], live[kCheckPerThread];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kCheckPerThread; ++k) {
       const int i = base + k * kValidateThreads + threadIdx.x;
-      page[k] = i < P ? __ldg(pt + i) : 0;
-      want[k] = i < P ? __ldg(ex + i) : 0u;
+      page[k] = i < max_pages ? __ldg(pt + i) : 0;
+      want[k] = i < max_pages ? __ldg(ex + i) : 0u;
+    }
+    if (P < 0) {
+      P = L > 0 ? (L + page_size - 1) / page_size : 0;
+      bad = P > max_pages || (P > 0 && num_pages <= 0);
+      if (bad || P == 0) break;  // from here on num_pages > 0: every gather index is valid
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = base + k * kValidateThreads + threadIdx.x;
-      if (i < P) {
-        if (page[k] < 0 || page[k] >= num_pages) bad = 1;
-        else if (__ldg(live_tags + page[k]) != want[k]) bad = 1;
-      }
+    for (int k = 0; k < kCheckPerThread; ++k) {
+      const bool in_range = page[k] >= 0 && page[k] < num_pages;
+      live[k] = __ldg(live_tags + (in_range ? page[k] : 0));
     }
+#pragma unroll
+    for (int k = 0; k < kCheckPerThread; ++k) {
+      const int i = base + k * kValidateThreads + threadIdx.x;
+      const bool in_range = page[k] >= 0 && page[k] < num_pages;
+      if (i < P && (!in_range || live[k] != want[k])) bad = 1;
+    }
+  }
+  if (P < 0) {  // an empty table (max_pages == 0): only the length can abort
+    P = L > 0 ? (L + page_size - 1) / page_size : 0;
+    bad = P > max_pages;
   }
   bad = __syncthreads_or(bad);
   if (threadIdx.x == 0) abort_mask[r] = static_cast<uint8_t>(bad != 0);
   return bad;
 }
 
+
+// The cache write and tag check of one decode step as one launch
+// (decode_step.cu); argument checks as fpk_decode_append_check_fp8.
+int append_check_entry(bool fp8, const void* k_new, const void* v_new, void* kv_pool,
+                       const float* k_scale, const float* v_scale, const int32_t* page_table,
+                       int32_t max_pages, const int32_t* seq_lens, const uint32_t* live_tags,
+                       const uint32_t* expected_tags, uint8_t* abort_mask, int32_t B, int32_t Hkv,
+                       int32_t D, int32_t page_size, int32_t num_pages, void* stream);
 
 }  // namespace fpk

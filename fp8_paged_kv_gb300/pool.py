@@ -14,8 +14,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (fpk_decode_append_check_bf16, fpk_decode_append_check_fp8,
-               fpk_decode_workspace_bytes, fpk_kv_append_bf16, fpk_kv_append_fp8,
+from . import (fpk_decode_append_check_bf16, fpk_decode_append_check_fp8, fpk_decode_step_bf16,
+               fpk_decode_step_fp8, fpk_decode_workspace_bytes, fpk_kv_append_bf16, fpk_kv_append_fp8,
                fpk_kv_prefill_bf16, fpk_kv_prefill_fp8, fpk_page_tags_bump,
                fpk_page_tags_validate, fpk_paged_decode_attn_bf16, fpk_paged_decode_attn_fp8)
 
@@ -161,20 +161,29 @@ class DecodePool:
     def step(self, validate: bool = True, stream=None):
         """One decode step.  With validation: the cache write and the batched tag
         check (one launch; a separate operation from attention), then attention
-        over the requests that passed.  Without it (the no-op tracker): the
-        write, then attention with no tag check.  With count_aborts the check
-        runs as its own launch so that it also produces the device-side count."""
+        over the requests that passed, launched as a programmatic dependent of
+        the check (fpk_decode_step_*).  Without it (the no-op tracker): the same
+        two launches with no tag check -- the write unguarded, attention over
+        every request.  With count_aborts the check runs as its own launch so
+        that it also produces the device-side count."""
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
-        if not validate:
-            self.append(stream=main)
-            self.attend(use_mask=False, stream=main)
-            return
-        if self.count_aborts:
+        if validate and self.count_aborts:
             self.append(stream=main)
             self.validate(stream=main)
+            self.attend(use_mask=True, stream=main)
+            return
+        wl = self.wl
+        kw = dict(Hkv=wl.Hkv, page_size=wl.page_size, num_pages=wl.num_pages,
+                  sm_scale=wl.sm_scale, num_splits=self.num_splits, stream=main)
+        tags = (self.live_tags, self.expected_tags, self.abort_mask) if validate else (None, None, None)
+        if self.fp8:
+            fpk_decode_step_fp8(self.k_new, self.v_new, self.kv_pool, self.k_scale, self.v_scale,
+                                self.page_table, self.seq_lens, *tags, self.q, self.out, self.lse,
+                                self.workspace, **kw)
         else:
-            self.append_check(stream=main)
-        self.attend(use_mask=True, stream=main)
+            fpk_decode_step_bf16(self.k_new, self.v_new, self.kv_pool, self.page_table,
+                                 self.seq_lens, *tags, self.q, self.out, self.lse, self.workspace,
+                                 **kw)
 
     # ------------------------------------------------------------- readback
     def pool_bytes(self):

@@ -210,8 +210,10 @@ int fpk_page_tags_validate(const int32_t* page_table, const uint32_t* expected_t
  * sicurezza della cache KV condivisa..."); sharing a launch with the write is
  * safe because the two touch disjoint data, and wherever the write refuses a
  * stale slot the check marks the same request for the same table entry.
- * abort_mask (uint8 [B]) is overwritten with the check's result; live_tags and
- * expected_tags are required.
+ * abort_mask (uint8 [B]) is overwritten with the check's result.  With
+ * live_tags and expected_tags both NULL (the no-op tracker) the launch only
+ * writes, unguarded, and abort_mask is not touched; one of them NULL is
+ * FPK_EINVAL.
  */
 int fpk_decode_append_check_fp8(const void* k_new, const void* v_new, uint8_t* kv_pool,
                                 const float* k_scale, const float* v_scale,
@@ -289,6 +291,38 @@ int fpk_paged_decode_attn_bf16(const void* q, const void* kv_pool,
                                int32_t num_splits, float sm_scale, int32_t B, int32_t Hq,
                                int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
                                void* stream);
+
+/*
+ * One whole decode step: fpk_decode_append_check_fp8 (the new token's write
+ * and the batched tag check, one launch) followed by
+ * fpk_paged_decode_attn_fp8 over the requests that passed, in the order the
+ * pages give (write, check before the decode operation reads, attend:
+ * "Cosa ha cambiato Cloudflare per Kimi e GLM" and "La sicurezza della cache
+ * KV condivisa...").  The check stays its own kernel; the attention kernel is
+ * launched as a programmatic dependent of it, so its set-up (work split,
+ * barriers) overlaps the check, and it reads the abort mask and the cache only
+ * once the check kernel has completed.  Arguments as in the two calls.  With
+ * live_tags and expected_tags both NULL (the no-op tracker) the step writes
+ * unguarded and attends every request, ignoring abort_mask.  All arguments
+ * are checked before anything is launched.
+ */
+int fpk_decode_step_fp8(const void* k_new, const void* v_new, uint8_t* kv_pool,
+                        const float* k_scale, const float* v_scale,
+                        const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                        const uint32_t* live_tags, const uint32_t* expected_tags,
+                        uint8_t* abort_mask, const void* q, float* out, float* lse,
+                        void* workspace, size_t workspace_bytes, int32_t num_splits,
+                        float sm_scale, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                        int32_t page_size, int32_t num_pages, void* stream);
+
+/* BF16-cache variant of fpk_decode_step_fp8 (no scales). */
+int fpk_decode_step_bf16(const void* k_new, const void* v_new, void* kv_pool,
+                         const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                         const uint32_t* live_tags, const uint32_t* expected_tags,
+                         uint8_t* abort_mask, const void* q, float* out, float* lse,
+                         void* workspace, size_t workspace_bytes, int32_t num_splits,
+                         float sm_scale, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t page_size, int32_t num_pages, void* stream);
 
 /*
  * Allocation-free variant of fpk_paged_decode_attn_fp8 (same arguments and
