@@ -29,6 +29,20 @@ int checked_launch_status() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int resident_grid(const void* kernel, int threads, size_t dyn_smem, int64_t want) {
+  if (want <= 0) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  const int sms = device_sm_count(dev);
+  if (want <= sms) return static_cast<int>(want);  // resident whatever the occupancy
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, dyn_smem) != cudaSuccess ||
+      per_sm <= 0 || sms <= 0)
+    return static_cast<int>(want < 1024 ? want : 1024);
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  return static_cast<int>(want < cap ? want : cap);
+}
+
 }  // namespace fpk
 
 extern "C" int fpk_version(void) { return 100; }

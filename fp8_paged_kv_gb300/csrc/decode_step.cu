@@ -35,8 +35,8 @@ __global__ void __launch_bounds__(kValidateThreads) append_check_kernel(WriteArg
     return;
   }
   const int64_t units = w.rows * w.Hkv * (w.D >> 3);
-  const float ks = kFp8 ? __ldg(w.k_scale) : 1.f;
-  const float vs = kFp8 ? __ldg(w.v_scale) : 1.f;
+  const Divisor ks = make_divisor(kFp8 ? __ldg(w.k_scale) : 1.f);
+  const Divisor vs = make_divisor(kFp8 ? __ldg(w.v_scale) : 1.f);
   const int64_t stride = static_cast<int64_t>(gridDim.x - nchk) * blockDim.x;
   for (int64_t u = static_cast<int64_t>(blockIdx.x - nchk) * blockDim.x + threadIdx.x; u < units;
        u += stride)

@@ -28,8 +28,8 @@ namespace {
 template <bool kFp8, bool kPrefill>
 __global__ void __launch_bounds__(256) write_tokens_kernel(WriteArgs a) {
   const int64_t units = a.rows * a.Hkv * (a.D >> 3);
-  const float ks = kFp8 ? __ldg(a.k_scale) : 1.f;
-  const float vs = kFp8 ? __ldg(a.v_scale) : 1.f;
+  const Divisor ks = make_divisor(kFp8 ? __ldg(a.k_scale) : 1.f);
+  const Divisor vs = make_divisor(kFp8 ? __ldg(a.v_scale) : 1.f);
   for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
        u += static_cast<int64_t>(gridDim.x) * blockDim.x)
     write_unit<kFp8, kPrefill>(a, u, ks, vs);
@@ -57,20 +57,170 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
 
 constexpr int kDimW = 128;          // head dimension (the only one supported)
 constexpr int kTileThreads = 256;   // 16 tokens x 16 groups of 8 dims
-constexpr int kTileMaxB = 8192;     // requests whose tile offsets fit in shared memory
+constexpr int kTileMaxB = 4096;     // requests whose offsets fit in shared memory
 
-__device__ __forceinline__ uint32_t quant_pair(uint32_t bf16x2, float s) {
-  const float a = __fdiv_rn(bf16_bits_to_float(static_cast<uint16_t>(bf16x2 & 0xFFFF)), s);
-  const float b = __fdiv_rn(bf16_bits_to_float(static_cast<uint16_t>(bf16x2 >> 16)), s);
+// e4m3 codes of the two bf16 values of a word (low half first); kFast takes
+// the corrected-product division (divisor with a normal reciprocal).
+template <bool kFast = false>
+__device__ __forceinline__ uint32_t quant_pair(uint32_t bf16x2, const Divisor& s) {
+  const float x0 = __uint_as_float(bf16x2 << 16), x1 = __uint_as_float(bf16x2 & 0xFFFF0000u);
+  const float a = kFast ? div_fast(x0, s) : div_by(x0, s);
+  const float b = kFast ? div_fast(x1, s) : div_by(x1, s);
   return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Prompt write, one CTA per (request, 16-token tile, kv head) unit in a
-// grid-stride loop.  The requests' first tile numbers are scanned into
-// shared memory once per CTA (s_tile0[r], r = 0..B).
+template <bool kFp8, bool kFast>
+__device__ __forceinline__ void prefill_units(const WriteArgs& a, const int* s_tile0, const int* s_row0,
+                                              int units, const Divisor& ks, const Divisor& vs,
+                                              int lane, int warp) {
+  const int tpp = a.page_size >> 4;
+  const int warps = kTileThreads / 32;
+  const int tk = lane >> 1, hk = (lane & 1) * 64;  // K: token, first dim
+  const int dv = 4 * lane;                          // V: first dim
+  // units < 2^31 (checked on the host): 32-bit index arithmetic
+  for (int u = static_cast<int>(blockIdx.x) * warps + warp; u < units; u += static_cast<int>(gridDim.x) * warps) {
+    const bool is_v = (u & 1) != 0;
+    const int th = u >> 1;
+    const int tile = th / a.Hkv;
+    const int h = th - tile * a.Hkv;
+    int lo = 0, hi = a.B - 1;  // the request: largest r with s_tile0[r] <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tile0[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int r = lo;
+    const int j = tile - s_tile0[r];
+    const int row0 = s_row0[r] + 16 * j;                // first source row of the tile
+    const int n = min(16, s_row0[r + 1] - row0);        // tokens in this tile
+    // guard loads (page id, then the two tags) ...
+    const int pi = (16 * j) / a.page_size;
+    const bool in_table = pi < a.max_pages;
+    const int page = in_table ? __ldg(a.page_table + static_cast<int64_t>(r) * a.max_pages + pi) : -1;
+    // ... while the source rows load: K as 8 x 16 bytes of one token, or V as
+    // 16 tokens x 8 bytes, in the same 32 registers
+    uint4 src[8];
+    if (!is_v) {
+      const uint16_t* ksrc = a.k_src + (static_cast<int64_t>(row0 + tk) * a.Hkv + h) * kDimW + hk;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        src[i] = tk < n ? __ldg(reinterpret_cast<const uint4*>(ksrc) + i) : make_uint4(0, 0, 0, 0);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const uint2 v = q < n ? __ldg(reinterpret_cast<const uint2*>(
+                                    a.v_src + (static_cast<int64_t>(row0 + q) * a.Hkv + h) * kDimW + dv))
+                              : make_uint2(0, 0);
+        if (q & 1) {
+          src[q >> 1].z = v.x;
+          src[q >> 1].w = v.y;
+        } else {
+          src[q >> 1].x = v.x;
+          src[q >> 1].y = v.y;
+        }
+      }
+    }
+    bool ok = in_table && page >= 0 && page < a.num_pages;
+    if (ok && a.live_tags != nullptr && a.expected_tags != nullptr)
+      ok = __ldg(a.live_tags + page) == __ldg(a.expected_tags + static_cast<int64_t>(r) * a.max_pages + pi);
+    if (!ok) {
+      if (lane == 0 && a.abort_mask != nullptr) a.abort_mask[r] = 1;
+      continue;
+    }
+    const uint4* kr = src;  // K part
+    // V part: token q's dims dv..dv+3 are (src[q/2].x, .y) for even q, (.z, .w) for odd q
+    auto vx = [&](int q) { return (q & 1) ? src[q >> 1].z : src[q >> 1].x; };
+    auto vy = [&](int q) { return (q & 1) ? src[q >> 1].w : src[q >> 1].y; };
+    const int64_t tb = ((static_cast<int64_t>(page) * a.Hkv + h) * tpp + (j % tpp)) * 2 * 16 * kDimW;
+    const int64_t vb = tb + 16 * kDimW;
+    if (kFp8) {
+      // K: 64 codes of token tk
+      if (!is_v && tk < n) {
+        uint4 w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w[i].x = quant_pair<kFast>(kr[2 * i].x, ks) | (quant_pair<kFast>(kr[2 * i].y, ks) << 16);
+          w[i].y = quant_pair<kFast>(kr[2 * i].z, ks) | (quant_pair<kFast>(kr[2 * i].w, ks) << 16);
+          w[i].z = quant_pair<kFast>(kr[2 * i + 1].x, ks) | (quant_pair<kFast>(kr[2 * i + 1].y, ks) << 16);
+          w[i].w = quant_pair<kFast>(kr[2 * i + 1].z, ks) | (quant_pair<kFast>(kr[2 * i + 1].w, ks) << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(a.kv_pool + tb + tk * kDimW + hk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = w[i];
+      }
+      // V: dims dv .. dv+3, tokens 0..15 -> four 16-byte dim rows
+      if (!is_v) continue;
+      uint32_t rows[4][4];
+#pragma unroll
+      for (int q = 0; q < 16; q += 2) {
+        // codes of tokens q, q+1 for dims dv, dv+1 (from x) and dv+2, dv+3 (from y)
+        const uint32_t lo0 = (vx(q) & 0xFFFFu) | (vx(q + 1) << 16);
+        const uint32_t hi0 = (vx(q) >> 16) | (vx(q + 1) & 0xFFFF0000u);
+        const uint32_t lo1 = (vy(q) & 0xFFFFu) | (vy(q + 1) << 16);
+        const uint32_t hi1 = (vy(q) >> 16) | (vy(q + 1) & 0xFFFF0000u);
+        const uint32_t c[4] = {quant_pair<kFast>(lo0, vs), quant_pair<kFast>(hi0, vs), quant_pair<kFast>(lo1, vs),
+                               quant_pair<kFast>(hi1, vs)};
+        const int wi = q >> 2, sh = (q & 2) * 8;  // word of the row, byte offset of token q
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+          if (sh == 0) rows[d][wi] = c[d];
+          else rows[d][wi] |= c[d] << 16;
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < 4; ++d) {
+        uint8_t* row = a.kv_pool + vb + (dv + d) * 16;
+        if (n == 16) {
+          *reinterpret_cast<uint4*>(row) = make_uint4(rows[d][0], rows[d][1], rows[d][2], rows[d][3]);
+        } else {
+          for (int q = 0; q < n; ++q) row[q] = static_cast<uint8_t>(rows[d][q >> 2] >> (8 * (q & 3)));
+        }
+      }
+    } else {
+      uint16_t* pool = reinterpret_cast<uint16_t*>(a.kv_pool);
+      if (!is_v && tk < n) {
+        uint4* dst = reinterpret_cast<uint4*>(pool + tb + tk * kDimW + hk);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = kr[i];
+      }
+      // V rows of 16 bf16: element (dim dv+d, token q)
+      if (!is_v) continue;
+#pragma unroll
+      for (int d = 0; d < 4; ++d) {
+        uint32_t w[8];
+#pragma unroll
+        for (int q = 0; q < 16; q += 2) {
+          const uint32_t e0 = d < 2 ? vx(q) : vy(q);
+          const uint32_t e1 = d < 2 ? vx(q + 1) : vy(q + 1);
+          const uint32_t b0 = (d & 1) ? (e0 >> 16) : (e0 & 0xFFFFu);
+          const uint32_t b1 = (d & 1) ? (e1 >> 16) : (e1 & 0xFFFFu);
+          w[q >> 1] = b0 | (b1 << 16);
+        }
+        uint16_t* row = pool + vb + (dv + d) * 16;
+        if (n == 16) {
+          reinterpret_cast<uint4*>(row)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(row)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+          for (int q = 0; q < n; ++q) row[q] = static_cast<uint16_t>(w[q >> 1] >> (16 * (q & 1)));
+        }
+      }
+    }
+  }
+}
+
+// Prompt write: one warp per (request, 16-token tile, kv head, K or V) unit,
+// in a grid-stride loop over the units (K/V, then kv head, fastest).  The requests' first
+// tile numbers and first source rows are scanned into shared memory once per
+// CTA; a unit's source loads are issued before its page guard resolves, and
+// only the stores wait for the guard.
+//   K: lane l writes token l/2, dims 64*(l&1) .. +63 (64 bytes of a 128-byte
+//      token row in e4m3, 128 bytes in bf16).
+//   V: lane l writes dims 4l .. 4l+3 over the 16 tokens (four dim rows of
+//      16 codes, or 16 bf16).
 template <bool kFp8>
 __global__ void __launch_bounds__(kTileThreads) prefill_tiles_kernel(WriteArgs a) {
-  extern __shared__ int s_tile0[];
+  extern __shared__ int s_meta[];  // [0, B]: first tile of request r; [B+1, 2B+2): first source row
+  int* s_tile0 = s_meta;
+  int* s_row0 = s_meta + a.B + 1;
   __shared__ int s_warp[kTileThreads / 32];
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
@@ -91,100 +241,25 @@ __global__ void __launch_bounds__(kTileThreads) prefill_tiles_kernel(WriteArgs a
   for (int i = 0; i < warp; ++i) before += s_warp[i];
   int run = before + incl - mine;
   for (int r = rb; r < re; ++r) {
+    const int c0 = __ldg(a.cu_seqlens + r);
     s_tile0[r] = run;
-    run += (__ldg(a.cu_seqlens + r + 1) - __ldg(a.cu_seqlens + r) + 15) >> 4;
+    s_row0[r] = c0;
+    run += (__ldg(a.cu_seqlens + r + 1) - c0 + 15) >> 4;
   }
-  if (t == kTileThreads - 1) s_tile0[a.B] = before + incl;
+  if (t == kTileThreads - 1) {
+    s_tile0[a.B] = before + incl;
+    s_row0[a.B] = __ldg(a.cu_seqlens + a.B);
+  }
   __syncthreads();
-  const int64_t units = static_cast<int64_t>(s_tile0[a.B]) * a.Hkv;
-  const float ks = kFp8 ? __ldg(a.k_scale) : 1.f;
-  const float vs = kFp8 ? __ldg(a.v_scale) : 1.f;
-  const int tpp = a.page_size >> 4;
-  // K: token tk, dims ck..ck+7.  V: tokens 4*qv..4*qv+3, dims 2*dv, 2*dv+1.
-  const int tk = t >> 4, ck = (t & 15) * 8;
-  const int qv = t & 3, dv = t >> 2;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    const int tile = static_cast<int>(u / a.Hkv);
-    const int h = static_cast<int>(u - static_cast<int64_t>(tile) * a.Hkv);
-    int lo = 0, hi = a.B - 1;  // the request: largest r with s_tile0[r] <= tile
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_tile0[mid] <= tile) lo = mid; else hi = mid - 1;
-    }
-    const int r = lo;
-    const int j = tile - s_tile0[r];
-    const int row0 = __ldg(a.cu_seqlens + r) + 16 * j;  // first source row of the tile
-    const int n = min(16, __ldg(a.cu_seqlens + r + 1) - row0);  // tokens in this tile
-    const int pi = (16 * j) / a.page_size;
-    bool ok = pi < a.max_pages;
-    int page = -1;
-    if (ok) {
-      page = __ldg(a.page_table + static_cast<int64_t>(r) * a.max_pages + pi);
-      ok = page >= 0 && page < a.num_pages;
-    }
-    if (ok && a.live_tags != nullptr && a.expected_tags != nullptr)
-      ok = __ldg(a.live_tags + page) == __ldg(a.expected_tags + static_cast<int64_t>(r) * a.max_pages + pi);
-    if (!ok) {
-      if (t == 0 && a.abort_mask != nullptr) a.abort_mask[r] = 1;
-      continue;
-    }
-    const int64_t tb = ((static_cast<int64_t>(page) * a.Hkv + h) * tpp + (j % tpp)) * 2 * 16 * kDimW;
-    const int64_t vb = tb + 16 * kDimW;
-    // K rows
-    if (tk < n) {
-      const int64_t src = (static_cast<int64_t>(row0 + tk) * a.Hkv + h) * kDimW + ck;
-      const uint4 kr = __ldg(reinterpret_cast<const uint4*>(a.k_src + src));
-      if (kFp8) {
-        const uint32_t w0 = quant_pair(kr.x, ks) | (quant_pair(kr.y, ks) << 16);
-        const uint32_t w1 = quant_pair(kr.z, ks) | (quant_pair(kr.w, ks) << 16);
-        *reinterpret_cast<uint2*>(a.kv_pool + tb + tk * kDimW + ck) = make_uint2(w0, w1);
-      } else {
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(a.kv_pool) + tb + tk * kDimW + ck) = kr;
-      }
-    }
-    // V columns: four tokens of two dims
-    uint32_t vw[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int tok = 4 * qv + q;
-      vw[q] = 0;
-      if (tok < n)
-        vw[q] = __ldg(reinterpret_cast<const uint32_t*>(
-            a.v_src + (static_cast<int64_t>(row0 + tok) * a.Hkv + h) * kDimW + 2 * dv));
-    }
-    const bool full = 4 * qv + 3 < n;
-    if (kFp8) {
-      // quant_pair(x) gives the codes of (dim 2dv, dim 2dv+1) of one token
-      const uint32_t c0 = quant_pair(vw[0], vs), c1 = quant_pair(vw[1], vs);
-      const uint32_t c2 = quant_pair(vw[2], vs), c3 = quant_pair(vw[3], vs);
-      const uint32_t row_a = (c0 & 0xFF) | ((c1 & 0xFF) << 8) | ((c2 & 0xFF) << 16) | ((c3 & 0xFF) << 24);
-      const uint32_t row_b = (c0 >> 8) | (c1 & 0xFF00) | ((c2 & 0xFF00) << 8) | ((c3 & 0xFF00) << 16);
-      uint8_t* pa = a.kv_pool + vb + (2 * dv) * 16 + 4 * qv;
-      uint8_t* pb = pa + 16;
-      if (full) {
-        *reinterpret_cast<uint32_t*>(pa) = row_a;
-        *reinterpret_cast<uint32_t*>(pb) = row_b;
-      } else {
-        for (int q = 0; q < 4 && 4 * qv + q < n; ++q) {
-          pa[q] = static_cast<uint8_t>(row_a >> (8 * q));
-          pb[q] = static_cast<uint8_t>(row_b >> (8 * q));
-        }
-      }
-    } else {
-      uint16_t* pa = reinterpret_cast<uint16_t*>(a.kv_pool) + vb + (2 * dv) * 16 + 4 * qv;
-      uint16_t* pb = pa + 16;
-      if (full) {
-        *reinterpret_cast<uint2*>(pa) = make_uint2((vw[0] & 0xFFFF) | (vw[1] << 16), (vw[2] & 0xFFFF) | (vw[3] << 16));
-        *reinterpret_cast<uint2*>(pb) = make_uint2((vw[0] >> 16) | (vw[1] & 0xFFFF0000u),
-                                                   (vw[2] >> 16) | (vw[3] & 0xFFFF0000u));
-      } else {
-        for (int q = 0; q < 4 && 4 * qv + q < n; ++q) {
-          pa[q] = static_cast<uint16_t>(vw[q] & 0xFFFF);
-          pb[q] = static_cast<uint16_t>(vw[q] >> 16);
-        }
-      }
-    }
-  }
+  const int units = s_tile0[a.B] * a.Hkv * 2;
+  const Divisor ks = make_divisor(kFp8 ? __ldg(a.k_scale) : 1.f);
+  const Divisor vs = make_divisor(kFp8 ? __ldg(a.v_scale) : 1.f);
+  // one division path for the whole kernel (uniform), so the unrolled body
+  // carries no per-element fallback
+  if (!kFp8 || (ks.recip_ok && vs.recip_ok))
+    prefill_units<kFp8, true>(a, s_tile0, s_row0, units, ks, vs, lane, warp);
+  else
+    prefill_units<kFp8, false>(a, s_tile0, s_row0, units, ks, vs, lane, warp);
 }
 
 // amax over the finite values of a bf16 tensor, as the largest |x| bit
@@ -253,18 +328,11 @@ int check_shapes(int B, int Hkv, int D, int page_size, int num_pages, int max_pa
 int launch_write(const WriteArgs& a, bool fp8, bool prefill, cudaStream_t s) {
   const int64_t units = a.rows * a.Hkv * (a.D >> 3);
   if (units == 0) return FPK_OK;
-  int dev = 0;
-  cudaGetDevice(&dev);
   const int64_t want = (units + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(device_sm_count(dev) > 0 ? device_sm_count(dev) : 132) * 16;
-  const int grid = static_cast<int>(want < cap ? want : cap);
-  if (fp8) {
-    if (prefill) write_tokens_kernel<true, true><<<grid, 256, 0, s>>>(a);
-    else write_tokens_kernel<true, false><<<grid, 256, 0, s>>>(a);
-  } else {
-    if (prefill) write_tokens_kernel<false, true><<<grid, 256, 0, s>>>(a);
-    else write_tokens_kernel<false, false><<<grid, 256, 0, s>>>(a);
-  }
+  auto kern = fp8 ? (prefill ? write_tokens_kernel<true, true> : write_tokens_kernel<true, false>)
+                  : (prefill ? write_tokens_kernel<false, true> : write_tokens_kernel<false, false>);
+  const int grid = resident_grid(reinterpret_cast<const void*>(kern), 256, 0, want);
+  kern<<<grid, 256, 0, s>>>(a);
   return checked_launch_status();
 }
 
@@ -301,17 +369,16 @@ int write_entry(bool fp8, bool prefill, const void* k, const void* v, const int3
   a.num_pages = num_pages;
   a.max_pages = max_pages;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (prefill && B <= kTileMaxB) {
+  // the tile-wise path indexes its units in 32 bits
+  const bool tile_path = prefill && B <= kTileMaxB &&
+                         ((rows + 15) / 16 + B) * static_cast<int64_t>(Hkv) * 2 < (int64_t(1) << 31);
+  if (tile_path) {
     // tile-wise prompt write (the per-token kernel below covers larger batches)
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const int sms = device_sm_count(dev) > 0 ? device_sm_count(dev) : 132;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    const int64_t want = (rows + 15) / 16 * Hkv + B * Hkv;  // an upper bound of the units
-    const int grid = static_cast<int>(want < cap ? want : cap);
-    const size_t smem = static_cast<size_t>(B + 1) * sizeof(int);
-    if (fp8) prefill_tiles_kernel<true><<<grid, kTileThreads, smem, s>>>(a);
-    else prefill_tiles_kernel<false><<<grid, kTileThreads, smem, s>>>(a);
+    const int64_t want = (((rows + 15) / 16 + B) * Hkv * 2 + 7) / 8;  // units, 8 warps per CTA
+    const size_t smem = static_cast<size_t>(2 * (B + 1)) * sizeof(int);
+    auto kern = fp8 ? prefill_tiles_kernel<true> : prefill_tiles_kernel<false>;
+    const int grid = resident_grid(reinterpret_cast<const void*>(kern), kTileThreads, smem, want);
+    kern<<<grid, kTileThreads, smem, s>>>(a);
     return checked_launch_status();
   }
   return launch_write(a, fp8, prefill, s);
@@ -371,11 +438,8 @@ extern "C" int fpk_quantize_e4m3(const float* x, const float* scale, uint8_t* ou
   if (n < 0) return FPK_EINVAL;
   if (n == 0) return FPK_OK;
   if (!x || !scale || !out) return FPK_EINVAL;
-  int dev = 0;
-  cudaGetDevice(&dev);
   const int64_t want = ((n >> 1) + 255) / 256 + 1;
-  const int64_t cap = static_cast<int64_t>(fpk::device_sm_count(dev) > 0 ? fpk::device_sm_count(dev) : 132) * 32;
-  const int grid = static_cast<int>(want < cap ? want : cap);
+  const int grid = fpk::resident_grid(reinterpret_cast<const void*>(fpk::quantize_kernel), 256, 0, want);
   fpk::quantize_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, scale, out, n);
   return fpk::checked_launch_status();
 }
@@ -386,12 +450,9 @@ extern "C" int fpk_amax_scale_bf16(const void* x, int64_t n, float* scale, uint3
   if (n > 0 && !fpk::aligned16(x)) return FPK_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return FPK_ECUDA;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int sms = fpk::device_sm_count(dev) > 0 ? fpk::device_sm_count(dev) : 132;
   const int64_t want = ((n >> 3) + 1023) / 1024;  // four 16-byte loads per thread
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
-  const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+  const int grid = fpk::resident_grid(reinterpret_cast<const void*>(fpk::amax_scale_kernel), 256, 0,
+                                      want < 1 ? 1 : want);
   fpk::amax_scale_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), n, scale, scratch);
   return fpk::checked_launch_status();
 }

@@ -37,7 +37,8 @@ __device__ __forceinline__ int request_of_row(const int32_t* cu, int B, int64_t 
 // Returns without writing (and marks the request aborted) when the
 // destination slot fails the guard.
 template <bool kFp8, bool kPrefill>
-__device__ __forceinline__ void write_unit(const WriteArgs& a, int64_t u, float ks, float vs) {
+__device__ __forceinline__ void write_unit(const WriteArgs& a, int64_t u, const Divisor& ks,
+                                           const Divisor& vs) {
   const int chunks = a.D >> 3;
   {
     const int c = static_cast<int>(u % chunks);
@@ -83,10 +84,10 @@ __device__ __forceinline__ void write_unit(const WriteArgs& a, int64_t u, float 
       uint8_t vq[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float k0 = __fdiv_rn(bf16_bits_to_float(kb[2 * i]), ks);
-        const float k1 = __fdiv_rn(bf16_bits_to_float(kb[2 * i + 1]), ks);
-        const float v0 = __fdiv_rn(bf16_bits_to_float(vb[2 * i]), vs);
-        const float v1 = __fdiv_rn(bf16_bits_to_float(vb[2 * i + 1]), vs);
+        const float k0 = div_by(bf16_bits_to_float(kb[2 * i]), ks);
+        const float k1 = div_by(bf16_bits_to_float(kb[2 * i + 1]), ks);
+        const float v0 = div_by(bf16_bits_to_float(vb[2 * i]), vs);
+        const float v1 = div_by(bf16_bits_to_float(vb[2 * i + 1]), vs);
         const uint16_t kp = __nv_cvt_float2_to_fp8x2(make_float2(k0, k1), __NV_SATFINITE, __NV_E4M3);
         const uint16_t vp = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
         if (i & 1) kw[i >> 1] |= static_cast<uint32_t>(kp) << 16; else kw[i >> 1] = kp;

@@ -13,7 +13,7 @@ import oracle
 from fp8_paged_kv_gb300 import (FpkError, fpk_amax_scale_bf16, fpk_kv_prefill_bf16,
                                 fpk_kv_prefill_fp8)
 from fp8_paged_kv_gb300.pool import NAN_BF16, NAN_E4M3, to_device
-from workloads import bf16_bits, custom
+from workloads import bf16_bits, bf16_to_f32, custom
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -147,3 +147,45 @@ def test_prefill_with_device_scales():
     got, _ = _run_prefill(wl, True, wl.page_table, wl.expected_tags, scales=(ks, vs))
     ref, _ = _oracle_prefill(wl, True, wl.page_table, wl.expected_tags, k_ref, v_ref)
     assert np.array_equal(got, ref)
+
+
+def _scales_under_test():
+    g = np.random.default_rng(2024)
+    s = [1.0, 3.0, 7.0, 0.1, 448.0, 1 / 448, 2.0 ** -30, 2.0 ** 30, 1e-30, 1e30, 2.0 ** -126,
+         2.0 ** -127, 2.0 ** -149, 3.0e38, np.finfo(np.float32).max]
+    s += [float(np.float32((2 - 2.0 ** -23) * 2.0 ** e)) for e in range(-24, 25, 3)]   # all-ones significands
+    s += [float(np.float32((1 + 2.0 ** -23) * 2.0 ** e)) for e in range(-24, 25, 3)]
+    s += list((2.0 ** g.uniform(-40, 40, 520)).astype(np.float32))
+    return [np.float32(v) for v in s]
+
+
+def test_quantiser_every_bf16_pattern_many_scales():
+    """The bf16-input quantiser of the cache writes (one reciprocal per tensor,
+    one corrected product per element) against the oracle's IEEE division:
+    every finite bf16 pattern, as K and as V, at ~570 scales including the
+    ones whose reciprocal is not a normal number."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    pats = pats[~np.isnan(bf16_to_f32(pats))]        # NaN inputs: compared elsewhere by NaN-ness
+    D, ps = 128, 16
+    T = -(-pats.size // D)
+    k = np.zeros(T * D, np.uint16)
+    k[:pats.size] = pats
+    k = k.reshape(T, 1, D)
+    v = np.ascontiguousarray(k[::-1])
+    P = -(-T // ps)
+    pt = np.arange(P, dtype=np.int32)[None, :]
+    cu = np.array([0, T], np.int32)
+    n = 2 * P * ps * D
+    k_d, v_d = to_device(k, DEV), to_device(v, DEV)
+    cu_d, pt_d = to_device(cu, DEV), to_device(pt, DEV)
+    pool = torch.zeros(n, dtype=torch.uint8, device=DEV)
+    sc_d = torch.empty(1, dtype=torch.float32, device=DEV)
+    for sc in _scales_under_test():
+        sc_d.fill_(float(sc))
+        fpk_kv_prefill_fp8(k_d, v_d, cu_d, pool, sc_d, sc_d, pt_d, None, None, None, Hkv=1, D=D,
+                           page_size=ps, num_pages=P)
+        ref = np.zeros(n, np.uint8)
+        oracle.kv_prefill(k, v, cu, ref, sc, sc, pt, None, None, None, fp8=True, Hkv=1, D=D,
+                          page_size=ps, num_pages=P)
+        got = pool.cpu().numpy()
+        assert np.array_equal(got, ref), f"scale {float(sc)!r}: {int((got != ref).sum())} codes differ"
