@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "step_ops.cuh"
 
 namespace fpk {
 

@@ -21,9 +21,6 @@ namespace fpk {
 int device_sm_count(int device);
 int checked_launch_status();
 bool aligned16(const void* p);
-// Grid for a grid-stride kernel: min(want, CTAs resident at once on the
-// current device), so that no CTA waits for another to finish its whole loop.
-int resident_grid(const void* kernel, int threads, size_t dyn_smem, int64_t want);
 
 // Status bits written into a workspace status word by the kernels.
 constexpr uint32_t kStatusWaitTimeout = 1u;   // a bounded wait gave up
@@ -53,40 +50,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Quotient x / s for a divisor used many times (the per-tensor quantiser
-// scale), by Markstein's division (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop. 34,
-// 1990): with r = RN(1/s), q0 = RN(x r) is within one ulp of x / s; the
-// residual x - q0 s is exact as one FMA, and RN(q0 + residual r) is the
-// correctly rounded quotient whenever it lies in the normal range.  Below
-// that (|x / s| < 2^-126) the result may differ from RN(x / s) by an ulp of a
-// subnormal -- far below 2^-10, where every such value encodes to a zero e4m3
-// code of the same sign.  Zero, infinite and NaN q0 are returned unchanged;
-// a divisor whose reciprocal is not a normal number takes the IEEE division.
-struct Divisor {
-  float s, r;
-  bool recip_ok;
-};
-__device__ __forceinline__ Divisor make_divisor(float s) {
-  Divisor d;
-  d.s = s;
-  d.r = __frcp_rn(s);
-  d.recip_ok = isfinite(d.r) && fabsf(d.r) >= 1.17549435e-38f;
-  return d;
-}
-// The corrected product alone, for a divisor with d.recip_ok.  A zero,
-// infinite or NaN q0 is the answer as it is (this keeps the sign of -0 and
-// the infinity of an overflowing quotient).
-__device__ __forceinline__ float div_fast(float x, const Divisor& d) {
-  const float q0 = __fmul_rn(x, d.r);
-  const float e = __fmaf_rn(-q0, d.s, x);
-  const float q = __fmaf_rn(e, d.r, q0);
-  return (q0 != 0.f && fabsf(q0) <= 3.40282347e38f) ? q : q0;
-}
-__device__ __forceinline__ float div_by(float x, const Divisor& d) {
-  return d.recip_ok ? div_fast(x, d) : __fdiv_rn(x, d.s);
 }
 
 // Programmatic dependent launch.  griddep_wait() returns once the grids this

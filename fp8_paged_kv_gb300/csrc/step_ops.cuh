@@ -4,6 +4,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "quant.cuh"
 
 namespace fpk {
 
@@ -164,6 +165,11 @@ __device__ __forceinline__ int check_request(const int32_t* __restrict__ page_ta
   return bad;
 }
 
+
+// Grid for a grid-stride kernel: min(want, CTAs resident at once on the
+// current device), so that no CTA waits for another to finish its whole loop
+// (api.cu).
+int resident_grid(const void* kernel, int threads, size_t dyn_smem, int64_t want);
 
 // The cache write and tag check of one decode step as one launch
 // (decode_step.cu); argument checks as fpk_decode_append_check_fp8.
