@@ -65,6 +65,10 @@ SIGNATURES = {
     "fpk_decode_step_bf16": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                             _SZ, _I32, _F, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "fpk_decode_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "fpk_w4_quantize": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _P]),
+    "fpk_w4_gemv": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P]),
+    "fpk_w8_quantize": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _P]),
+    "fpk_w8_gemv": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I32, _I32, _P]),
 }
 
 _lock = threading.Lock()
@@ -327,3 +331,34 @@ def fpk_decode_status(workspace, stream=None) -> int:
     _check(load_library().fpk_decode_status(_ptr(workspace, _U8, "workspace"), ctypes.byref(v),
                                             _stream(stream)), "fpk_decode_status")
     return int(v.value)
+
+
+# ---------------------------------------------------------------- weight GEMV
+def fpk_w4_quantize(w, codes, scales, stream=None):
+    N, K = w.shape
+    _check(load_library().fpk_w4_quantize(_ptr(w, _BF16_LIKE, "w"), _ptr(codes, _U8, "codes"),
+                                          _ptr(scales, _BF16_LIKE, "scales"), N, K, _stream(stream)),
+           "fpk_w4_quantize")
+
+
+def fpk_w4_gemv(x, codes, scales, y, stream=None):
+    B, K = x.shape
+    N = y.shape[1]
+    _check(load_library().fpk_w4_gemv(_ptr(x, _BF16_LIKE, "x"), _ptr(codes, _U8, "codes"),
+                                      _ptr(scales, _BF16_LIKE, "scales"), _ptr(y, _F32, "y"), B, N, K,
+                                      _stream(stream)), "fpk_w4_gemv")
+
+
+def fpk_w8_quantize(w, codes, row_scales, stream=None):
+    N, K = w.shape
+    _check(load_library().fpk_w8_quantize(_ptr(w, _BF16_LIKE, "w"), _ptr(codes, _U8, "codes"),
+                                          _ptr(row_scales, _F32, "row_scales"), N, K, _stream(stream)),
+           "fpk_w8_quantize")
+
+
+def fpk_w8_gemv(x, codes, row_scales, y, stream=None):
+    B, K = x.shape
+    N = y.shape[1]
+    _check(load_library().fpk_w8_gemv(_ptr(x, _BF16_LIKE, "x"), _ptr(codes, _U8, "codes"),
+                                      _ptr(row_scales, _F32, "row_scales"), _ptr(y, _F32, "y"), B, N, K,
+                                      _stream(stream)), "fpk_w8_gemv")

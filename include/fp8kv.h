@@ -88,6 +88,43 @@ extern "C" {
 #define FPK_ENOSPC 3
 #define FPK_ECUDA 4
 
+/* ------------------------------------------------------------------------
+ * Weight-only quantised decode GEMV (the pages' second technique: "La
+ * compressione dei pesi GLM modifica il compromesso tra le fasi", remio.ai --
+ * GLM 5.2's weights went from FP8 to INT4 because decode streams every weight
+ * from HBM at each step; INT4 weights are expanded before the multiply).  The
+ * pages give no format; this one is the library's own:
+ *
+ *   W [N][K] bf16 (N % 16 == 0, K % 128 == 0) is cut into slices of 16 rows x
+ *   128 k, stored slice-row-block major: slice (n / 16, k / 128).
+ *   INT4: per row and group of 128 k, scale s = bf16(amax / 7) over the
+ *     group's finite values; code q = clamp(rint(w / s), -8, 7) (fp32 IEEE
+ *     division, ties to even), 0 for a non-finite w or s == 0; stored as the
+ *     nibble q + 8.  Dequantised weight q * s.  A slice is 1024 bytes: byte
+ *     512*h + 16*l + 4*u + (0..3) holds word u of row 8*h + l/4 (l = 0..31);
+ *     nibble p (bits 4p..4p+3) of word u is k = 16*v + 4*(l % 4) + i with
+ *     v = 2u + ((p >> 1) & 1), i = 2*(p & 1) + (p >> 2).
+ *     codes: N*K/2 bytes; scales: bf16 [N][K/128] (row-major).
+ *   e4m3: per row, scale r = amax / 448 over the row's finite values (1 if
+ *     that amax is 0); codes e4m3(w / r) as the cache quantiser.  A slice is
+ *     2048 bytes: byte 1024*h + 512*c + 16*l + b holds row 8*h + l/4,
+ *     k = 16*(4c + b/4) + 4*(l % 4) + b % 4.  codes: N*K bytes; row_scales:
+ *     float [N].
+ *
+ * y[b][n] = sum_k x[b][k] * Wq[n][k] for b < B, 1 <= B <= 16 (decode tokens);
+ * x bf16 [B][K] (16-byte aligned), y float [B][N].  Accumulation is fp32 on
+ * the tensor cores; for K > 2048 the K chunks are added into y with atomics
+ * (y is zeroed by the call first), so the last bits of y may vary between
+ * calls.  B > 16 returns FPK_EUNSUPPORTED.
+ * ------------------------------------------------------------------------ */
+int fpk_w4_quantize(const void* w, uint8_t* codes, void* scales, int32_t N, int32_t K, void* stream);
+int fpk_w4_gemv(const void* x, const uint8_t* codes, const void* scales, float* y, int32_t B,
+                int32_t N, int32_t K, void* stream);
+int fpk_w8_quantize(const void* w, uint8_t* codes, float* row_scales, int32_t N, int32_t K,
+                    void* stream);
+int fpk_w8_gemv(const void* x, const uint8_t* codes, const float* row_scales, float* y, int32_t B,
+                int32_t N, int32_t K, void* stream);
+
 /* Library ABI version (major * 100 + minor). */
 int fpk_version(void);
 

@@ -63,6 +63,12 @@ def _load():
             lib.orc_quantize_bf16_array.argtypes = [_P, _I64, _F, _P]
             lib.orc_amax_scale_bf16.restype = _F
             lib.orc_amax_scale_bf16.argtypes = [_P, _I64]
+            lib.orc_w4_quantize.argtypes = [_P, _I, _I, _P, _P]
+            lib.orc_w8_quantize.argtypes = [_P, _I, _I, _P, _P]
+            lib.orc_w4_pack.argtypes = [_P, _I, _I, _P]
+            lib.orc_w8_pack.argtypes = [_P, _I, _I, _P]
+            lib.orc_w4_gemv.argtypes = [_P, _I, _P, _P, _I, _I, _P]
+            lib.orc_w8_gemv.argtypes = [_P, _I, _P, _P, _I, _I, _P]
             lib.orc_kv_append.argtypes = [_P, _P, _I, _P, _F, _F, _P, _I, _P,
                                           _P, _P, _P, _I, _I, _I, _I, _I]
             lib.orc_kv_prefill.argtypes = [_P, _P, _P, _I, _P, _F, _F, _P, _I,
@@ -206,3 +212,69 @@ def dense_attention(q, K, V, sm_scale: float):
     _load().orc_dense_attention(_ptr(qd), _ptr(Kd), _ptr(Vd), L, D, float(sm_scale),
                                 _ptr(scores), _ptr(out), ctypes.byref(lse))
     return out, lse.value
+
+
+# --------------------------------------------------------------------------
+# weight-only quantised GEMV
+# --------------------------------------------------------------------------
+
+def w4_quantize(w_bits):
+    """INT4 codes q [N][K] (int8 in [-8, 7]) and bf16 scales [N][K/128], natural layout."""
+    w = _c(w_bits, np.uint16)
+    N, K = w.shape
+    q = np.empty((N, K), np.int8)
+    sc = np.empty((N, K // 128), np.uint16)
+    _load().orc_w4_quantize(_ptr(w), N, K, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def w8_quantize(w_bits):
+    """e4m3 codes [N][K] and fp32 row scales [N], natural layout."""
+    w = _c(w_bits, np.uint16)
+    N, K = w.shape
+    c = np.empty((N, K), np.uint8)
+    r = np.empty(N, np.float32)
+    _load().orc_w8_quantize(_ptr(w), N, K, _ptr(c), _ptr(r))
+    return c, r
+
+
+def w4_pack(q):
+    """INT4 codes in the slice layout (the library's weight format)."""
+    q = _c(q, np.int8)
+    N, K = q.shape
+    out = np.zeros(N * K // 2, np.uint8)
+    _load().orc_w4_pack(_ptr(q), N, K, _ptr(out))
+    return out
+
+
+def w8_pack(codes):
+    """e4m3 codes in the slice layout."""
+    c = _c(codes, np.uint8)
+    N, K = c.shape
+    out = np.zeros(N * K, np.uint8)
+    _load().orc_w8_pack(_ptr(c), N, K, _ptr(out))
+    return out
+
+
+def w4_gemv(x_bits, q, scales):
+    """y [B][N] = x . (q * s)^T in fp64."""
+    x = _c(x_bits, np.uint16)
+    q = _c(q, np.int8)
+    sc = _c(scales, np.uint16)
+    B, K = x.shape
+    N = q.shape[0]
+    y = np.empty((B, N), np.float64)
+    _load().orc_w4_gemv(_ptr(x), B, _ptr(q), _ptr(sc), N, K, _ptr(y))
+    return y
+
+
+def w8_gemv(x_bits, codes, row_scales):
+    """y [B][N] = x . (decode(codes) * r)^T in fp64."""
+    x = _c(x_bits, np.uint16)
+    c = _c(codes, np.uint8)
+    r = _c(row_scales, np.float32)
+    B, K = x.shape
+    N = c.shape[0]
+    y = np.empty((B, N), np.float64)
+    _load().orc_w8_gemv(_ptr(x), B, _ptr(c), _ptr(r), N, K, _ptr(y))
+    return y

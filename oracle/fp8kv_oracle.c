@@ -437,3 +437,146 @@ void orc_dense_attention(const double *q, const double *K, const double *V, int 
     }
     *lse = m + log(z);
 }
+
+/* ------------------------------------------------------------------------- */
+/* weight-only quantised GEMV (the pages' second technique)                   */
+/* ------------------------------------------------------------------------- */
+/*
+ * "La compressione dei pesi GLM modifica il compromesso tra le fasi"
+ * (remio.ai): GLM 5.2's weights went from FP8 to INT4 for decode, where every
+ * weight is read from memory at each step.  The pages give no format; the
+ * readings taken (groups of 128 along K with a bf16 scale amax / 7 and codes
+ * rint(w / s) clamped to [-8, 7]; e4m3 weights with an fp32 scale
+ * amax / 448 per row) are restated here from their definitions.
+ */
+
+/* float -> bf16 bits, round to nearest even (NaN -> quiet NaN). */
+static uint16_t bf16_round(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return (uint16_t)((u >> 16) | 0x40u);
+    return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
+/* INT4: q [N][K] in [-8, 7] and bf16 scales [N][K/128], natural layout. */
+void orc_w4_quantize(const uint16_t *w, int N, int K, int8_t *q, uint16_t *scales)
+{
+    int n, g, k, G = K / 128;
+    for (n = 0; n < N; ++n) {
+        for (g = 0; g < G; ++g) {
+            double amax = 0.0;
+            volatile float af, sq;
+            float sf;
+            uint16_t sb;
+            for (k = 128 * g; k < 128 * (g + 1); ++k) {
+                double x = (double)bf16_bits_to_float(w[(int64_t)n * K + k]);
+                if (isfinite(x) && fabs(x) > amax) amax = fabs(x);
+            }
+            af = (float)amax;
+            sq = af / 7.0f;
+            sb = bf16_round(sq);
+            scales[(int64_t)n * G + g] = sb;
+            sf = bf16_bits_to_float(sb);
+            for (k = 128 * g; k < 128 * (g + 1); ++k) {
+                float x = bf16_bits_to_float(w[(int64_t)n * K + k]);
+                int code = 0;
+                if (sf != 0.0f && isfinite(x)) {
+                    volatile float r = x / sf;
+                    float v = nearbyintf(r);
+                    code = v > 7.0f ? 7 : v < -8.0f ? -8 : (int)v;
+                }
+                q[(int64_t)n * K + k] = (int8_t)code;
+            }
+        }
+    }
+}
+
+/* e4m3 weights: codes [N][K] and fp32 row scales [N], natural layout. */
+void orc_w8_quantize(const uint16_t *w, int N, int K, uint8_t *codes, float *row_scales)
+{
+    int n, k;
+    for (n = 0; n < N; ++n) {
+        double amax = 0.0;
+        volatile float af, r;
+        for (k = 0; k < K; ++k) {
+            double x = (double)bf16_bits_to_float(w[(int64_t)n * K + k]);
+            if (isfinite(x) && fabs(x) > amax) amax = fabs(x);
+        }
+        af = (float)amax;
+        r = amax == 0.0 ? 1.0f : af / 448.0f;
+        row_scales[n] = r;
+        for (k = 0; k < K; ++k)
+            codes[(int64_t)n * K + k] = orc_quantize_bf16(w[(int64_t)n * K + k], r);
+    }
+}
+
+/* The INT4 slice layout, written from its definition: byte
+ * 512h + 16l + 4u + p/2 of slice (s, g) holds, in its low (p even) or high
+ * nibble, element (16s + 8h + l/4, 128g + 16(2u + ((p>>1)&1)) + 4(l%4) + 2(p&1) + (p>>2)). */
+void orc_w4_pack(const int8_t *q, int N, int K, uint8_t *out)
+{
+    int s, g, h, l, u, p, G = K / 128;
+    for (s = 0; s < N / 16; ++s)
+        for (g = 0; g < G; ++g)
+            for (h = 0; h < 2; ++h)
+                for (l = 0; l < 32; ++l)
+                    for (u = 0; u < 4; ++u)
+                        for (p = 0; p < 8; ++p) {
+                            int row = 16 * s + 8 * h + l / 4;
+                            int k = 128 * g + 16 * (2 * u + ((p >> 1) & 1)) + 4 * (l % 4) + 2 * (p & 1) + (p >> 2);
+                            uint8_t nib = (uint8_t)(q[(int64_t)row * K + k] + 8);
+                            int64_t byte = ((int64_t)s * G + g) * 1024 + 512 * h + 16 * l + 4 * u + p / 2;
+                            if ((p & 1) == 0) out[byte] = (uint8_t)((out[byte] & 0xF0) | nib);
+                            else out[byte] = (uint8_t)((out[byte] & 0x0F) | (nib << 4));
+                        }
+}
+
+/* The e4m3 slice layout: byte 1024h + 512c + 16l + b of slice (s, g) holds
+ * element (16s + 8h + l/4, 128g + 16(4c + b/4) + 4(l%4) + b%4). */
+void orc_w8_pack(const uint8_t *codes, int N, int K, uint8_t *out)
+{
+    int s, g, h, c, l, b, G = K / 128;
+    for (s = 0; s < N / 16; ++s)
+        for (g = 0; g < G; ++g)
+            for (h = 0; h < 2; ++h)
+                for (c = 0; c < 2; ++c)
+                    for (l = 0; l < 32; ++l)
+                        for (b = 0; b < 16; ++b) {
+                            int row = 16 * s + 8 * h + l / 4;
+                            int k = 128 * g + 16 * (4 * c + b / 4) + 4 * (l % 4) + b % 4;
+                            out[((int64_t)s * G + g) * 2048 + 1024 * h + 512 * c + 16 * l + b] =
+                                codes[(int64_t)row * K + k];
+                        }
+}
+
+/* y[b][n] = sum_k x[b][k] * q[n][k] * s[n][k/128], in fp64. */
+void orc_w4_gemv(const uint16_t *x, int B, const int8_t *q, const uint16_t *scales, int N, int K,
+                 double *y)
+{
+    int b, n, k, G = K / 128;
+    for (b = 0; b < B; ++b)
+        for (n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (k = 0; k < K; ++k)
+                acc += (double)bf16_bits_to_float(x[(int64_t)b * K + k]) * (double)q[(int64_t)n * K + k] *
+                       (double)bf16_bits_to_float(scales[(int64_t)n * G + k / 128]);
+            y[(int64_t)b * N + n] = acc;
+        }
+}
+
+/* y[b][n] = sum_k x[b][k] * decode(code[n][k]) * r[n], in fp64. */
+void orc_w8_gemv(const uint16_t *x, int B, const uint8_t *codes, const float *row_scales, int N, int K,
+                 double *y)
+{
+    int b, n, k;
+    for (b = 0; b < B; ++b)
+        for (n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (k = 0; k < K; ++k)
+                acc += (double)bf16_bits_to_float(x[(int64_t)b * K + k]) *
+                       orc_e4m3_decode(codes[(int64_t)n * K + k]);
+            y[(int64_t)b * N + n] = acc * (double)row_scales[n];
+        }
+}
