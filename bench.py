@@ -10,6 +10,7 @@ identical values for comparison.  Prints ONE JSON line on rank 0.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload b32_8k]
   python bench.py --impl reference ...     # the CPU oracle, timed on host cores
   python bench.py --capacity [--kv-budget-gib 4]   # admission curve, BF16 vs FP8 cache
+  python bench.py --gemv [--gemv-n 28672 --gemv-k 8192]   # INT4 vs e4m3 weight decode GEMV
 
 Multi-GPU (torchrun): every rank runs an independent replica (its own requests
 and pool); nothing on the data path is exchanged, only the timing is reduced.
@@ -537,6 +538,64 @@ def run_capacity(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
+def run_gemv(args, rank, world):
+    """Weight-only quantised decode GEMV (the pages' second technique): INT4
+    weights in groups of 128 against e4m3 weights with a row scale, for one
+    N x K projection (random-init bf16 weights, synthetic activations) at
+    decode batches of 1..16 tokens.  L2 is flushed before every timed launch
+    (the INT4 weights alone would fit in it)."""
+    import fp8_paged_kv_gb300 as fpk
+    from fp8_paged_kv_gb300 import build as fbuild
+    if rank == 0 or world == 1:
+        fbuild.build()
+    barrier(world)
+    fpk.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    N, K = args.gemv_n, args.gemv_k
+    g = torch.Generator(device=dev)
+    g.manual_seed(11 + rank)
+    w = (torch.randn(N, K, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    c4 = torch.empty(N * K // 2, dtype=torch.uint8, device=dev)
+    s4 = torch.empty(N, K // 128, dtype=torch.bfloat16, device=dev)
+    c8 = torch.empty(N * K, dtype=torch.uint8, device=dev)
+    r8 = torch.empty(N, dtype=torch.float32, device=dev)
+    fpk.fpk_w4_quantize(w, c4, s4)
+    fpk.fpk_w8_quantize(w, c8, r8)
+    del w
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev)
+    peak, peak_kind = measured_peaks()
+    pts = []
+    with ClockSampler(local_rank()) as clk:
+        for B in (1, 2, 4, 8, 16):
+            x = torch.randn(B, K, device=dev, generator=g).to(torch.bfloat16)
+            y = torch.empty(B, N, device=dev)
+            row = {"batch": B}
+            for name, fn, wbytes in (("int4", lambda: fpk.fpk_w4_gemv(x, c4, s4, y), N * K // 2 + N * (K // 128) * 2),
+                                     ("fp8", lambda: fpk.fpk_w8_gemv(x, c8, r8, y), N * K + N * 4)):
+                t = []
+                for i in range(3 + args.capacity_reps):
+                    flush.zero_()
+                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    fn()
+                    e.record(s)
+                    torch.cuda.synchronize(dev)
+                    if i >= 3:
+                        t.append(a.elapsed_time(e))
+                ms = statistics.median(t)
+                nbytes = wbytes + B * K * 2 + B * N * 4
+                row[name] = {"us": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                             "frac": nbytes / (ms * 1e-3) / 1e9 / peak, "bytes": nbytes}
+            row["int4_speedup"] = row["fp8"]["us"] / row["int4"]["us"]
+            pts.append(row)
+    line = {"mode": "gemv", "shape": f"N={N}, K={K}, random-init bf16 weights", "points": pts,
+            "peak_gbs": peak, "peak_source": peak_kind,
+            "l2": "flushed (512 MB write) before every timed launch", "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def local_rank() -> int:
     return int(os.environ.get("LOCAL_RANK", "0"))
 
@@ -554,6 +613,10 @@ def main():
                     help="admission curve at a fixed KV budget instead of the step benchmark")
     ap.add_argument("--kv-budget-gib", type=float, default=4.0)
     ap.add_argument("--capacity-reps", type=int, default=10)
+    ap.add_argument("--gemv", action="store_true",
+                    help="INT4 vs e4m3 weight-only decode GEMV instead of the step benchmark")
+    ap.add_argument("--gemv-n", type=int, default=28672)
+    ap.add_argument("--gemv-k", type=int, default=8192)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -563,6 +626,9 @@ def main():
         return
     if args.capacity:
         run_capacity(args, rank, world)
+        return
+    if args.gemv:
+        run_gemv(args, rank, world)
         return
 
     import fp8_paged_kv_gb300 as fpk

@@ -2,13 +2,15 @@
 e4m3 with a row scale as the comparison).
 
 Quantiser output (codes in the slice layout and scales) bit-exact against the
-oracle; y within a bound derived from the arithmetic: every product x * q
-(or x * e4m3 value) is exact in fp32, the tensor cores sum 16 of them per
-step in fp32, a group's 8 steps are summed in fp32, scaled once, and the
-K/128 group sums (and the split-K chunks) are added in fp32.  Each output
-therefore carries at most (8 + 1 + K/128 + 2) roundings of relative size
-2^-24 (2^-23 if the tensor core truncates) on a sum bounded by sum_k |w x|:
-|y - y_ref| <= 4 (16 + K/128) 2^-24 sum_k |w_k x_k|.
+oracle; y within a bound derived from the arithmetic.  The activations enter
+the tensor cores as the bf16 values they are and the weights as exact bf16
+(an INT4 code, or an e4m3 value), so every product is exact in fp32; the
+tensor cores sum 16 per step in fp32, a group's 8 steps are summed in fp32,
+scaled once, and the K/128 group sums (and the split-K chunks) are added in
+fp32: at most (8 + 1 + K/128 + 2) roundings of relative size 2^-24 (2^-23 if
+the tensor core truncates) on a sum bounded by sum_k |w x|:
+|y - y_ref| <= 4 (16 + K/128) 2^-24 sum_k |w_k x_k|  (plus a 2^-30 max|x|
+sum_k |w_k| allowance for results near the bottom of the fp32 range).
 """
 import numpy as np
 import pytest
@@ -70,7 +72,9 @@ def test_w8_quantiser_bit_exact(N, K):
 
 
 def _tol(wd, x, K):
-    return 4 * (16 + K / 128) * 2.0 ** -24 * (np.abs(x) @ np.abs(wd).T) + 1e-30
+    xmax = np.abs(x).max(axis=1, keepdims=True)
+    return (4 * (16 + K / 128) * 2.0 ** -24 * (np.abs(x) @ np.abs(wd).T)
+            + 2.0 ** -30 * xmax * np.abs(wd).sum(axis=1)[None, :] + 1e-30)
 
 
 @pytest.mark.parametrize("B", [1, 3, 8, 9, 16])
@@ -102,6 +106,36 @@ def test_w8_gemv_within_bound(B, N, K):
     ref = oracle.w8_gemv(xb, c, r)
     wd = oracle.e4m3_decode(c) * r.astype(np.float64)[:, None]
     got = y.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= _tol(wd, bf16_to_f32(xb).astype(np.float64), K))
+
+
+@pytest.mark.parametrize("w4", [True, False])
+def test_gemv_activation_range(w4):
+    # rows of very different magnitude (far beyond the f16 range) and a zero row
+    N, K, B = 64, 2176, 4
+    wb = _weights(3, N, K)
+    g = np.random.default_rng(9)
+    x = g.standard_normal((B, K)).astype(np.float32)
+    x[0] *= 1e20
+    x[1] *= 1e-20
+    x[2] = 0
+    x[3, :100] *= 1e5
+    xb = bf16_bits(x)
+    y = torch.full((B, N), float("nan"), device=DEV)
+    if w4:
+        codes, scales = _gpu_w4(wb)
+        fpk_w4_gemv(to_device(xb, DEV), codes, scales, y)
+        q, sc = oracle.w4_quantize(wb)
+        ref = oracle.w4_gemv(xb, q, sc)
+        wd = q.astype(np.float64) * np.repeat(bf16_to_f32(sc).astype(np.float64), 128, axis=1)
+    else:
+        codes, rs = _gpu_w8(wb)
+        fpk_w8_gemv(to_device(xb, DEV), codes, rs, y)
+        c, r = oracle.w8_quantize(wb)
+        ref = oracle.w8_gemv(xb, c, r)
+        wd = oracle.e4m3_decode(c) * r.astype(np.float64)[:, None]
+    got = y.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got)) and not got[2].any()
     assert np.all(np.abs(got - ref) <= _tol(wd, bf16_to_f32(xb).astype(np.float64), K))
 
 
