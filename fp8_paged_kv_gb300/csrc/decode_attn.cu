@@ -49,32 +49,48 @@ constexpr int kTile = 16;        // tokens per tile
 constexpr int kDim = 128;        // head dimension
 constexpr int kGroupMax = 8;     // query heads per kv head (N of the MMA tile)
 constexpr int kMergeStride = 132;  // floats per head row of the merge buffer
+constexpr int kMergeBars = 6;      // merge_free, cbar, the three rounds of the two-slot merge, the four-slot one
+constexpr int64_t kInflightBudget = 26ll << 20;  // bytes of ring stages over the grid (see Cfg)
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 static_assert(kConsumerWarps * 32 == 128, "the split-segment combine gives each consumer thread one of the 128 dims");
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <bool kFp8>
+template <bool kFp8, bool kDeep = false>
 struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kBlockBytes = kTile * kDim * kElem;  // one K (or V) tile
   // a stage holds two consecutive tiles, each as it lies in the pool:
   // [K tile 0][V tile 0][K tile 1][V tile 1]
   static constexpr int kStageBytes = 4 * kBlockBytes;
-  static constexpr int kStages = kFp8 ? 8 : 4;
+  // Ring depth: kStages stages in shared memory, of which a launch uses all or
+  // kStagesShallow.  Deeper rings keep more copies in flight per CTA, which
+  // pays while the whole grid's copies in flight stay under kInflightBudget;
+  // beyond it (measured on GB300: about 26 MiB over the GPU) the memory
+  // system serves the copies more slowly than with the shallower ring.  The
+  // deep FP8 variant holds 12 stages; the others hold only the shallow ring
+  // (a larger shared-memory footprint costs a little even when unused).
+  static constexpr int kStages = kFp8 ? (kDeep ? 12 : 8) : 4;
+  static constexpr int kStagesShallow = kFp8 ? 8 : 4;
   // Within a segment piece consumer warp c takes stages c, c+4, ...; with
-  // kStages a multiple of the warp count, the previous round of a stage was
+  // the depth a multiple of the warp count, the previous round of a stage was
   // consumed by the same warp, so no warp ever waits on a stage's mbarrier
   // while its previous phase is still pending (the parity test would alias
   // two phases back).  Across pieces the merge barrier gives the same order.
-  static_assert(kStages % kConsumerWarps == 0, "ring stages must be a multiple of the consumer warps");
+  static_assert(kStages % kConsumerWarps == 0 && kStagesShallow % kConsumerWarps == 0,
+                "ring depths must be multiples of the consumer warps");
+  static_assert(kStages <= 16, "a producer batch gives each stage two lanes");
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kMergeBytes = kConsumerWarps * kGroupMax * kMergeStride * 4;
+  // (m, l, O) slots of the merge of the consumer warps' results: four (one
+  // round), or two (two rounds) in the deep variant, whose ring leaves no
+  // room for four at two CTAs per SM.
+  static constexpr int kMergeSlots = kDeep ? 2 : 4;
+  static constexpr int kMergeBytes = kMergeSlots * kGroupMax * kMergeStride * 4;
   // (m, l) per warp and head, then one fault flag per warp; rounded to 16 bytes
   // so that the mbarriers that follow stay 8-byte aligned for any warp count
   static constexpr int kMlBytes = (kConsumerWarps * kGroupMax * 4 * 2 + kConsumerWarps * 4 + 15) / 16 * 16;
-  static constexpr int kBarBytes = (2 * kStages + 3) * 8;
+  static constexpr int kBarBytes = (2 * kStages + kMergeBars) * 8;
   static constexpr int kSmemBytes = kRingBytes + kMergeBytes + kMlBytes + kBarBytes + kStages * 4 + 64;
 };
 
@@ -183,17 +199,17 @@ __device__ __forceinline__ int token_of_row(int i) {
   return 4 * ((i & 7) >> 1) + (i & 1) + 2 * (i >> 3);
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kDeep>
 __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const AttnArgs a) {
-  using C = Cfg<kFp8>;
+  using C = Cfg<kFp8, kDeep>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;
   float* s_o = reinterpret_cast<float*>(smem + C::kRingBytes);
-  float* s_m = s_o + kConsumerWarps * kGroupMax * kMergeStride;
+  float* s_m = s_o + C::kMergeSlots * kGroupMax * kMergeStride;
   float* s_l = s_m + kConsumerWarps * kGroupMax;
   int* s_wfault = reinterpret_cast<int*>(s_l + kConsumerWarps * kGroupMax);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kMergeBytes + C::kMlBytes);
-  int* s_stage_fault = reinterpret_cast<int*>(bars + 2 * C::kStages + 3);
+  int* s_stage_fault = reinterpret_cast<int*>(bars + 2 * C::kStages + kMergeBars);
 
   __shared__ int64_t s_warp_sum[kThreads / 32];
   __shared__ int s_warp_nz[kThreads / 32], s_warp_min[kThreads / 32], s_warp_max[kThreads / 32];
@@ -268,6 +284,11 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   const int64_t b0 = s0 * T / W;
   const int64_t b1 = s1 * T / W;
   const bool has_work = b0 < b1;  // uniform over the CTA
+  // ring depth of this launch, from the CTAs that have work
+  int64_t active = W < nctas ? W : nctas;
+  if (T < active) active = T;
+  const uint32_t depth =
+      active * C::kStages * C::kStageBytes <= kInflightBudget ? C::kStages : C::kStagesShallow;
   if (has_work && mine > 0 && b0 >= excl * a.Hkv && b0 < (excl + mine) * a.Hkv) {
     int64_t base = excl * a.Hkv;
     for (int r = rb; r < re; ++r) {
@@ -287,17 +308,23 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   // barriers
   const uint32_t full0 = smem_addr(bars);
   const uint32_t empty0 = full0 + 8 * C::kStages;
-  const uint32_t merge_full = full0 + 16 * C::kStages;
-  const uint32_t merge_free = merge_full + 8;
+  const uint32_t merge_free = full0 + 16 * C::kStages;
   const uint32_t cbar = merge_free + 8;  // consumer-warp barrier of the split-segment combine
+  // the two-slot merge of a piece: warps 2, 3 have filled slots 0, 1 (mrg0);
+  // warps 0, 1 have read them (mrg1); warps 0, 1 have filled them (mrg2).
+  // The four-slot merge: every warp has filled its slot (mrg4).
+  const uint32_t mrg0 = cbar + 8, mrg1 = cbar + 16, mrg2 = cbar + 24, mrg4 = cbar + 32;
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(merge_full, kConsumerWarps);
     mbar_init(merge_free, kConsumerWarps);
     mbar_init(cbar, kConsumerWarps);
+    mbar_init(mrg0, 2);
+    mbar_init(mrg1, 2);
+    mbar_init(mrg2, 2);
+    mbar_init(mrg4, kConsumerWarps);
     fence_barrier_init();
   }
   __syncthreads();
@@ -346,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     // Stages are issued the moment they are free, so the ring never drains at
     // a batch boundary, and a batch only waits on stages that an earlier batch
     // filled.  Page ids of the next batch of a piece load while this one polls.
-    constexpr int kBatch = C::kStages < 16 ? C::kStages : 16;
+    const int batch = static_cast<int>(depth);  // a batch never wraps around the ring
     const uint64_t pol = l2_policy_evict_first();
     const int si = lane >> 1;  // stage slot of this lane within a batch
     const int ci = lane & 1;   // tile of the stage this lane copies
@@ -361,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       const int nst = (p.t1 - p.t0 + 1) >> 1;
       auto load_id = [&](int k0) {
         int pg = -1;
-        if (si < kBatch && k0 + si < nst) {
+        if (si < batch && k0 + si < nst) {
           const int t = p.t0 + 2 * (k0 + si) + ci;
           if (t < p.t1) pg = __ldg(ptrow + t / tpp);
         }
@@ -373,9 +400,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         ab = is_aborted(a, p.r);
       }
       if (ab) continue;  // the consumers skip it too
-      for (int k0 = 0; k0 < nst && ok; k0 += kBatch) {
-        const int cnt = min(kBatch, nst - k0);
-        const int nxt = load_id(k0 + kBatch);  // prefetch (unused past the piece)
+      for (int k0 = 0; k0 < nst && ok; k0 += batch) {
+        const int cnt = min(batch, nst - k0);
+        const int nxt = load_id(k0 + batch);  // prefetch (unused past the piece)
         const bool member = si < cnt;
         const int tA = p.t0 + 2 * (k0 + si);
         const bool hasB = tA + 1 < p.t1;
@@ -385,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         const bool okB = hasB && pgB >= 0 && pgB < a.num_pages;
         const bool pair = okA && okB && tA / tpp == (tA + 1) / tpp;  // adjacent tiles of one page
         const uint32_t jj = j + si;
-        const uint32_t stage = jj % C::kStages;
-        const uint32_t round = jj / C::kStages;
+        const uint32_t stage = jj % depth;
+        const uint32_t round = jj / depth;
         const uint32_t fb = full0 + 8 * stage;
         bool todo = member;
         bool ready = false;
@@ -436,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     }
     if (!ok && lane == 0) {
       // give in-flight copies (bounded) time to land before the CTA exits
-      for (uint32_t s = 0; s < C::kStages && s < j; ++s) {
-        const uint32_t issued = (j - 1 - s) / C::kStages + 1;
+      for (uint32_t s = 0; s < depth && s < j; ++s) {
+        const uint32_t issued = (j - 1 - s) / depth + 1;
         mbar_wait(full0 + 8 * s, (issued - 1) & 1, a.status);
       }
     }
@@ -446,6 +473,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
 
   // ======================= consumer warps =======================
   const int c = warp - 1;
+  constexpr int nslots = C::kMergeSlots;
+  static_assert(nslots == kConsumerWarps || nslots == 2, "the merge takes four slots or two");
+  float* const s_mo = s_o;
   const int g = lane >> 2;   // MMA group id: A row / B column
   const int t4 = lane & 3;   // thread in group
   const int rowA = token_of_row(g);  // token of fragment row g (row g+8 is rowA + 2)
@@ -497,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       return mb.seg + (mb.dense ? mb.w0 + i : worker_of(mb.xseg + i, T, W));
     };
     float2* s_w = reinterpret_cast<float2*>(s_o);
-    constexpr int kChunk = kConsumerWarps * kGroupMax * kMergeStride / (2 * kGroupMax);
+    constexpr int kChunk = C::kMergeSlots * kGroupMax * kMergeStride / (2 * kGroupMax);
     float* s_M = s_m;              // running maximum per head
     float* s_r = s_m + kGroupMax;  // rescale of the running sums by this chunk
     float* s_W = s_l;              // running sum of weights per head
@@ -720,10 +750,17 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     int fault = 0;
     const int nst = (ntiles + 1) >> 1;  // stages of this piece, two tiles each
 
+    // ring position of stage k of this piece, advanced by the warp count
+    uint32_t stage = (jbase + c) % depth;
+    uint32_t round = (jbase + c) / depth;
     for (int k = c; k < nst; k += kConsumerWarps) {
-      const uint32_t j = jbase + k;
-      const uint32_t stage = j % C::kStages;
-      const uint32_t round = j / C::kStages;
+      if (k != c) {
+        stage += kConsumerWarps;
+        if (stage >= depth) {
+          stage -= depth;
+          ++round;
+        }
+      }
       const bool got = mbar_wait(full0 + 8 * stage, round & 1, a.status);
       if (!__all_sync(kFull, got)) {
         ok = false;
@@ -889,7 +926,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     jbase += nst;
     if (!ok) break;
 
-    // ---- merge the consumer warps' (m, l, O) of this piece
+    // ---- merge the consumer warps' (m, l, O) of this piece.  Four slots:
+    // every warp fills its own and the output loop below combines them.  Two
+    // slots: warps 2, 3 are folded into warps 0, 1, whose results go back
+    // into the two slots for the output loop.
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(kFull, l0, off);
@@ -900,8 +940,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       const bool got = mbar_wait(merge_free, (piece_idx - 1) & 1, a.status);
       if (!__all_sync(kFull, got)) break;
     }
-    {
-      float* mo = s_o + c * kGroupMax * kMergeStride;
+    // this lane's (m, l, O) into slot sl
+    auto put = [&](int sl) {
+      float* mo = s_mo + sl * kGroupMax * kMergeStride;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         mo[(2 * t4) * kMergeStride + 16 * mt + g] = o[mt][0];
@@ -910,39 +951,81 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         mo[(2 * t4 + 1) * kMergeStride + 16 * mt + g + 8] = o[mt][3];
       }
       if (g == 0) {
-        s_m[c * kGroupMax + 2 * t4] = m0;
-        s_m[c * kGroupMax + 2 * t4 + 1] = m1;
-        s_l[c * kGroupMax + 2 * t4] = l0;
-        s_l[c * kGroupMax + 2 * t4 + 1] = l1;
+        s_m[sl * kGroupMax + 2 * t4] = m0;
+        s_m[sl * kGroupMax + 2 * t4 + 1] = m1;
+        s_l[sl * kGroupMax + 2 * t4] = l0;
+        s_l[sl * kGroupMax + 2 * t4 + 1] = l1;
       }
-      if (lane == 0) s_wfault[c] = fault;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(merge_full);
+      if (lane == 0) s_wfault[sl] = fault;
+      __syncwarp();
+    };
+    // log-sum-exp of slot sl's (m, l, O) into this lane's
+    auto take = [&](int sl) {
+      const float* mo = s_mo + sl * kGroupMax * kMergeStride;
+      const float n0 = s_m[sl * kGroupMax + 2 * t4], n1 = s_m[sl * kGroupMax + 2 * t4 + 1];
+      const float M0 = fmaxf(m0, n0), M1 = fmaxf(m1, n1);
+      const float a0 = m0 == kNegInf ? 0.f : fast_exp2(m0 - M0), a1 = m1 == kNegInf ? 0.f : fast_exp2(m1 - M1);
+      const float b0 = n0 == kNegInf ? 0.f : fast_exp2(n0 - M0), b1 = n1 == kNegInf ? 0.f : fast_exp2(n1 - M1);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] = fmaf(mo[(2 * t4) * kMergeStride + 16 * mt + g], b0, o[mt][0] * a0);
+        o[mt][1] = fmaf(mo[(2 * t4 + 1) * kMergeStride + 16 * mt + g], b1, o[mt][1] * a1);
+        o[mt][2] = fmaf(mo[(2 * t4) * kMergeStride + 16 * mt + g + 8], b0, o[mt][2] * a0);
+        o[mt][3] = fmaf(mo[(2 * t4 + 1) * kMergeStride + 16 * mt + g + 8], b1, o[mt][3] * a1);
+      }
+      l0 = fmaf(s_l[sl * kGroupMax + 2 * t4], b0, l0 * a0);
+      l1 = fmaf(s_l[sl * kGroupMax + 2 * t4 + 1], b1, l1 * a1);
+      m0 = M0;
+      m1 = M1;
+      fault |= s_wfault[sl];
+      __syncwarp();  // every lane has read the slot before any lane writes it
+    };
+    auto arrive_wait = [&](uint32_t arrive_bar, uint32_t wait_bar) -> bool {
+      if (arrive_bar != 0u && lane == 0) mbar_arrive(arrive_bar);
+      if (wait_bar == 0u) return true;
+      return __all_sync(kFull, mbar_wait(wait_bar, piece_idx & 1, a.status));
+    };
     {
-      const bool got = mbar_wait(merge_full, piece_idx & 1, a.status);
-      if (!__all_sync(kFull, got)) break;
+      bool got = true;
+      if constexpr (nslots == kConsumerWarps) {
+        put(c);
+        got = arrive_wait(mrg4, mrg4);
+      } else if (c >= 2) {
+        put(c - 2);
+        got = arrive_wait(mrg0, mrg2);
+      } else {
+        got = arrive_wait(0u, mrg0);
+        if (got) {
+          take(c);
+          got = arrive_wait(mrg1, mrg1);  // both slots read before either is rewritten
+          if (got) {
+            put(c);
+            got = arrive_wait(mrg2, mrg2);
+          }
+        }
+      }
+      if (!got) break;
     }
     const int seg = p.r * a.Hkv + p.h;
     const bool whole = p.t0 == 0 && p.t1 == p.n;
     const int ct = ct_all;
     int anyfault = 0;
 #pragma unroll
-    for (int k = 0; k < kConsumerWarps; ++k) anyfault |= s_wfault[k];
+    for (int k = 0; k < nslots; ++k) anyfault |= s_wfault[k];
     for (int idx = ct; idx < a.G * kDim; idx += kConsumerWarps * 32) {
       const int hd = idx >> 7;
       const int d = idx & (kDim - 1);
       float M = kNegInf;
 #pragma unroll
-      for (int k = 0; k < kConsumerWarps; ++k) M = fmaxf(M, s_m[k * kGroupMax + hd]);
+      for (int k = 0; k < nslots; ++k) M = fmaxf(M, s_m[k * kGroupMax + hd]);
       const bool dead = anyfault || M == kNegInf;
       float wsum = 0.f, acc = 0.f;
 #pragma unroll
-      for (int k = 0; k < kConsumerWarps; ++k) {
+      for (int k = 0; k < nslots; ++k) {
         const float mk = s_m[k * kGroupMax + hd];
         const float f = mk == kNegInf ? 0.f : fast_exp2(mk - M);
-        wsum += s_l[k * kGroupMax + hd] * f;
-        acc += s_o[(k * kGroupMax + hd) * kMergeStride + d] * f;
+        wsum = fmaf(s_l[k * kGroupMax + hd], f, wsum);
+        acc = fmaf(s_mo[(k * kGroupMax + hd) * kMergeStride + d], f, acc);
       }
       if (whole) {
         const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
@@ -965,19 +1048,18 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
 // host side
 // ---------------------------------------------------------------------------
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_auto_ctas[2][kMaxDevices];  // resident CTAs per SM, per variant
+std::atomic<int> g_auto_ctas[3][kMaxDevices];  // resident CTAs per SM: BF16, FP8, deep FP8
 
-template <bool kFp8>
+template <bool kFp8, bool kDeep = false>
 int prepare_kernel(int dev) {
-  std::atomic<int>& slot = g_auto_ctas[kFp8 ? 1 : 0][dev];
+  std::atomic<int>& slot = g_auto_ctas[kDeep ? 2 : kFp8 ? 1 : 0][dev];
   int v = slot.load(std::memory_order_relaxed);
   if (v > 0) return v;
-  auto kern = paged_decode_split_kernel<kFp8>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kFp8>::kSmemBytes) !=
-      cudaSuccess)
-    return -1;
+  auto kern = paged_decode_split_kernel<kFp8, kDeep>;
+  constexpr int smem = Cfg<kFp8, kDeep>::kSmemBytes;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Cfg<kFp8>::kSmemBytes) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) !=
           cudaSuccess ||
       per_sm <= 0)
     return -1;
@@ -1033,6 +1115,47 @@ int check_attn_shapes(int B, int Hq, int Hkv, int D, int page_size, int num_page
 
 enum class AttnLaunch { kPlain, kCheckOnly, kAfterStepWrite };
 
+// The deep-ring FP8 variant pays when the CTAs that will have work keep no
+// more than kInflightBudget of stages in flight: a grid of at most W CTAs, or
+// the whole-segment mode, which the kernel takes for a uniform batch of
+// between 3/4 of the CTAs and all of them segments (the host cannot see the
+// context lengths; if they turn out uneven, the deep variant runs with its
+// shallow ring).  It must also fit as many CTAs per SM as the shallow one.
+bool deep_ring(int dev, int W, int ctas, int B, int Hkv, bool auto_split) {
+  using D = Cfg<true, true>;
+  const int64_t segs = static_cast<int64_t>(B) * Hkv;
+  int64_t active = W < ctas ? W : ctas;
+  if (auto_split && 4 * segs >= 3 * static_cast<int64_t>(ctas) && segs <= ctas) active = segs;
+  if (active * D::kStages * D::kStageBytes > kInflightBudget) return false;
+  const int deep = prepare_kernel<true, true>(dev);
+  return deep > 0 && deep >= prepare_kernel<true, false>(dev);
+}
+
+template <bool kFp8, bool kDeep>
+int launch_split_kernel(const AttnArgs& a, int dev, int ctas, cudaStream_t s, bool after_step_write) {
+  constexpr int smem = Cfg<kFp8, kDeep>::kSmemBytes;
+  if (prepare_kernel<kFp8, kDeep>(dev) <= 0) return FPK_ECUDA;  // sets the kernel's shared-memory size
+  if (!after_step_write) {
+    paged_decode_split_kernel<kFp8, kDeep><<<ctas, kThreads, smem, s>>>(a);
+    return checked_launch_status();
+  }
+  // launched as a programmatic dependent of the step's write + check kernel:
+  // its set-up overlaps that kernel; it reads the mask and the cache only
+  // after griddep_wait()
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<kFp8, kDeep>, a) != cudaSuccess) return FPK_ECUDA;
+  return checked_launch_status();
+}
+
 template <bool kFp8>
 int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
                const float* v_scale, const int32_t* page_table, int32_t max_pages,
@@ -1086,25 +1209,9 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
   a.sm_scale_log2 = sm_scale * kLog2e;
   if (mode == AttnLaunch::kCheckOnly) return FPK_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (mode == AttnLaunch::kPlain) {
-    paged_decode_split_kernel<kFp8><<<ctas, kThreads, Cfg<kFp8>::kSmemBytes, s>>>(a);
-    return checked_launch_status();
-  }
-  // launched as a programmatic dependent of the step's write + check kernel:
-  // its set-up overlaps that kernel; it reads the mask and the cache only
-  // after griddep_wait()
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<kFp8>::kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<kFp8>, a) != cudaSuccess) return FPK_ECUDA;
-  return checked_launch_status();
+  if (kFp8 && deep_ring(dev, W, ctas, B, Hkv, num_splits == 0))
+    return launch_split_kernel<true, true>(a, dev, ctas, s, mode == AttnLaunch::kAfterStepWrite);
+  return launch_split_kernel<kFp8, false>(a, dev, ctas, s, mode == AttnLaunch::kAfterStepWrite);
 }
 
 }  // namespace
