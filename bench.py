@@ -424,33 +424,21 @@ def time_prefill(pool, reps: int = 5):
 
 def time_e2e(pool, steps: int, warmup: int):
     """Same step through the public API with host buffers: pinned H2D of the step's
-    inputs (q, new K/V rows, context lengths), the step, D2H of out/lse/abort mask."""
-    wl = pool.wl
-    s = torch.cuda.current_stream()
-    h_q = pool.q.cpu().pin_memory()
-    h_k = pool.k_new.cpu().pin_memory()
-    h_v = pool.v_new.cpu().pin_memory()
-    h_len = pool.seq_lens.cpu().pin_memory()
-    h_out = torch.empty_like(pool.out, device="cpu").pin_memory()
-    h_lse = torch.empty_like(pool.lse, device="cpu").pin_memory()
-    h_mask = torch.empty_like(pool.abort_mask, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_len))
-    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_mask))
+    inputs (q, new K/V rows, context lengths: one buffer, one copy), the step, D2H of
+    out/lse/abort mask (one buffer, one copy)."""
+    h_in = pool.io_in.cpu().pin_memory()
+    h_out = torch.empty_like(pool.io_out, device="cpu").pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
 
     def h2d_copies():
-        pool.q.copy_(h_q, non_blocking=True)
-        pool.k_new.copy_(h_k, non_blocking=True)
-        pool.v_new.copy_(h_v, non_blocking=True)
-        pool.seq_lens.copy_(h_len, non_blocking=True)
+        pool.io_in.copy_(h_in, non_blocking=True)
 
     def d2h_copies():
-        h_out.copy_(pool.out, non_blocking=True)
-        h_lse.copy_(pool.lse, non_blocking=True)
-        h_mask.copy_(pool.abort_mask, non_blocking=True)
+        h_out.copy_(pool.io_out, non_blocking=True)
 
     g = capture_step(pool, True, io=(h2d_copies, d2h_copies))
     ms = time_graph(g, steps, warmup)
-    del s
     return ms, h2d, d2h
 
 

@@ -33,6 +33,23 @@ def to_device(a: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(a).to(device)
 
 
+def _arena(device, specs):
+    """One device buffer holding several tensors, each at a 256-byte aligned
+    offset, so that a step's inputs (or results) move between host and device
+    in one copy.  Returns (buffer, {name: view})."""
+    offs, total = [], 0
+    for _, shape, dtype in specs:
+        total = (total + 255) // 256 * 256
+        offs.append(total)
+        total += int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    buf = torch.zeros(max(total, 1), dtype=torch.uint8, device=device)
+    views = {}
+    for (name, shape, dtype), off in zip(specs, offs):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        views[name] = buf[off:off + n].view(dtype).view(shape)
+    return buf, views
+
+
 class DecodePool:
     def __init__(self, wl, fp8: bool = True, device="cuda", num_splits: int | None = None):
         self.wl = wl
@@ -49,17 +66,22 @@ class DecodePool:
         self.expected_tags = to_device(wl.expected_tags, dev)
         self.k_scale = torch.tensor([float(wl.k_scale)], dtype=torch.float32, device=dev)
         self.v_scale = torch.tensor([float(wl.v_scale)], dtype=torch.float32, device=dev)
-        self.seq_lens = to_device(wl.prompt_lens.astype(np.int32), dev)
-        self.abort_mask = torch.zeros(wl.B, dtype=torch.uint8, device=dev)
+        # a step's inputs and results, each in one buffer (io_in, io_out)
+        self.io_in, v_in = _arena(dev, [("q", (wl.B, wl.Hq, wl.D), torch.bfloat16),
+                                        ("k_new", (wl.B, wl.Hkv, wl.D), torch.bfloat16),
+                                        ("v_new", (wl.B, wl.Hkv, wl.D), torch.bfloat16),
+                                        ("seq_lens", (wl.B,), torch.int32)])
+        self.io_out, v_out = _arena(dev, [("out", (wl.B, wl.Hq, wl.D), torch.float32),
+                                          ("lse", (wl.B, wl.Hq), torch.float32),
+                                          ("abort_mask", (wl.B,), torch.uint8)])
+        self.q, self.k_new, self.v_new, self.seq_lens = (v_in[k] for k in ("q", "k_new", "v_new", "seq_lens"))
+        self.out, self.lse, self.abort_mask = (v_out[k] for k in ("out", "lse", "abort_mask"))
+        self.seq_lens.copy_(to_device(wl.prompt_lens.astype(np.int32), dev))
+        self.q.copy_(to_device(wl.q, dev))
         self.abort_count = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.q = to_device(wl.q, dev)
-        self.out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((wl.B, wl.Hq), dtype=torch.float32, device=dev)
         self.num_splits = wl.num_splits if num_splits is None else num_splits
         ws = fpk_decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, self.num_splits)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
-        self.k_new = None
-        self.v_new = None
         self.count_aborts = True
 
     @property
