@@ -84,6 +84,18 @@ def test_uniform_batch_one_segment_per_cta(fp8, abort_one):
     assert_attention_close(out, lse, ro, rl, f"uniform fp8={fp8} abort={abort_one}")
 
 
+@pytest.mark.parametrize("fp8", [True, False])
+def test_uneven_batch_of_whole_segment_size(fp8):
+    # 30 x 8 segments, as above, but of uneven lengths: the host launches the
+    # deep-ring FP8 variant for a batch that may run one whole segment per CTA;
+    # the kernel finds the lengths uneven, splits over a full wave and then
+    # runs only the shallow part of its ring, with the two-slot merge
+    lens = list(rng_for(84, "lens").integers(1, 400, size=30))
+    wl = custom(84, B=30, Hq=16, Hkv=8, ps=16, prompt_lens=lens, steps=0)
+    out, lse, ro, rl = _run_case(wl, fp8, 0)
+    assert_attention_close(out, lse, ro, rl, f"uneven fp8={fp8}")
+
+
 def test_split_invariance():
     lens = [3000, 1, 900]
     wl = custom(80, B=3, Hq=32, Hkv=4, ps=32, prompt_lens=lens, steps=0)
