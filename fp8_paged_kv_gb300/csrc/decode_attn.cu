@@ -861,9 +861,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         m1 = mn1;
       }
       const float base0 = m0 == kNegInf ? 0.f : m0, base1 = m1 == kNegInf ? 0.f : m1;
-      // ---- P^T as the B operand of O^T = V^T P^T, per tile
-      // (bf16 keeps only 8 significant bits, so the bf16 cache multiplies V by
-      // P = hi + lo, two bf16 parts; f16 P is exact enough for the FP8 cache)
+      // ---- P^T as the B operand of O^T = V^T P^T, per tile, as P = hi + lo:
+      // two f16 (FP8 cache) or bf16 (BF16 cache) parts.  One f16 P alone
+      // errs by up to 2^-12 of each p, which reaches the 2e-3 absolute
+      // tolerance on outlier channels where the output is small against |V|.
       uint32_t pb[2][2], pl[2][2];
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
@@ -875,8 +876,12 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         const uint32_t pr1 = kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3);
         pb[tt][0] = movmatrix_trans(pr0);
         pb[tt][1] = movmatrix_trans(pr1);
-        pl[tt][0] = pl[tt][1] = 0u;
-        if (!kFp8) {
+        if (kFp8) {
+          const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&pr0));
+          const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&pr1));
+          pl[tt][0] = movmatrix_trans(pack_f16x2(p0 - h0.x, p1 - h0.y));
+          pl[tt][1] = movmatrix_trans(pack_f16x2(p2 - h1.x, p3 - h1.y));
+        } else {
           pl[tt][0] = movmatrix_trans(pack_bf16x2(p0 - __uint_as_float(pr0 << 16),
                                                   p1 - __uint_as_float(pr0 & 0xffff0000u)));
           pl[tt][1] = movmatrix_trans(pack_bf16x2(p2 - __uint_as_float(pr1 << 16),
@@ -900,6 +905,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
             e4m3x4_to_f16x4(va, af[0], af[2]);
             e4m3x4_to_f16x4(vb, af[1], af[3]);
             mma_f16(o[mt], af, pb[tt][0], pb[tt][1]);
+            mma_f16(o[mt], af, pl[tt][0], pl[tt][1]);
           } else {
             const uint8_t* Vs = Sb + (2 * tt + 1) * C::kBlockBytes;
             const uint2 va = *reinterpret_cast<const uint2*>(Vs + (16 * mt + g) * 32 + 8 * t4);

@@ -50,7 +50,7 @@ def _run_case(wl, fp8, num_splits, abort=None, use_mask=True, pt_override=None):
 
 @pytest.mark.parametrize("fp8", [True, False])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-@pytest.mark.parametrize("ps", [16, 64])
+@pytest.mark.parametrize("ps", [16, 32, 64, 128, 256])
 def test_small_ragged(fp8, G, ps):
     Hkv = 2
     lens = [0, 1, 15, 16, 17, 100, 3 * ps + 7, 257]
@@ -94,6 +94,30 @@ def test_uneven_batch_of_whole_segment_size(fp8):
     wl = custom(84, B=30, Hq=16, Hkv=8, ps=16, prompt_lens=lens, steps=0)
     out, lse, ro, rl = _run_case(wl, fp8, 0)
     assert_attention_close(out, lse, ro, rl, f"uneven fp8={fp8}")
+
+
+@pytest.mark.parametrize("case", ["uniform", "uneven", "splits200", "splits4096"])
+def test_repeated_launches_bit_identical(case):
+    # the partition, each CTA's merge order and each segment's combine order
+    # are fixed, whichever CTA arrives last: repeated launches must agree to
+    # the bit (a race between the copy ring and its readers would not)
+    if case == "uniform":
+        lens, ns = [700] * 30, 0
+    elif case == "uneven":
+        lens, ns = list(rng_for(85, "lens").integers(1, 1400, size=30)), 0
+    else:
+        lens, ns = list(rng_for(86, "lens").integers(1, 3000, size=12)), int(case[6:])
+    wl = custom(87, B=len(lens), Hq=16, Hkv=8, ps=16, prompt_lens=lens, steps=0)
+    pool = DecodePool(wl, fp8=True, device=DEV, num_splits=ns)
+    pool.prefill()
+    pool.attend()
+    first = pool.out.clone(), pool.lse.clone()
+    for _ in range(20):
+        pool.out.fill_(float("nan"))
+        pool.attend()
+        assert torch.equal(pool.out.view(torch.int32), first[0].view(torch.int32))
+        assert torch.equal(pool.lse.view(torch.int32), first[1].view(torch.int32))
+    assert pool.workspace[:4].view(torch.int32).item() == 0
 
 
 def test_split_invariance():
