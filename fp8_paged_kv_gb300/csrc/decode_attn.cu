@@ -185,6 +185,14 @@ __device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, int64_t
   return true;
 }
 
+// Four 8 x 8 matrices of 16-bit elements from shared memory (ldmatrix).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
@@ -789,10 +797,15 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
           kr[tt][1] = lds128(Ks + rowA * kDim + 64 + 16 * t4);
           kr[tt][2] = lds128(Ks + (rowA + 2) * kDim + 16 * t4);
           kr[tt][3] = lds128(Ks + (rowA + 2) * kDim + 64 + 16 * t4);
+          // V operand words by ldmatrix: four 8 x 8 b16 blocks of dim rows
+          // (16 bytes each) per load; lane 8i + r gives the address of row r
+          // of block i, and lane 4g + t receives bytes 4t .. 4t+3 of row g of
+          // every block, i.e. tokens 4t .. 4t+3 of one dim
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            vr[tt][mt][0] = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g) * 16 + 4 * t4);
-            vr[tt][mt][1] = *reinterpret_cast<const uint32_t*>(Vs + (16 * mt + g + 8) * 16 + 4 * t4);
+          for (int mt = 0; mt < 8; mt += 2) {
+            const int dim = 16 * mt + 8 * (lane >> 3) + (lane & 7);
+            ldmatrix_x4(smem_addr(Vs + dim * 16), vr[tt][mt][0], vr[tt][mt][1], vr[tt][mt + 1][0],
+                        vr[tt][mt + 1][1]);
           }
         }
         __syncwarp();
