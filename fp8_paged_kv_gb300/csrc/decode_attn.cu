@@ -223,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   __shared__ int s_warp_nz[kThreads / 32], s_warp_min[kThreads / 32], s_warp_max[kThreads / 32];
   __shared__ int s_start[4];
   __shared__ int s_last;
+  __shared__ Piece s_pend_piece;  // the pending arrivals of split pieces (see publish_partial)
+  __shared__ int s_pend_seg, s_pend_k;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   }
   if (tid == 0) {
     s_start[0] = -1;
+    s_pend_k = 0;
   }
   __syncthreads();
   int64_t before = 0, total = 0;
@@ -510,11 +513,11 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   // CTA is fenced first; returns 1 for the arrival that completes `count`,
   // 0 for the others, -1 if a barrier gave up.  Nothing ever waits on another
   // CTA.
-  auto ticket = [&](int* ctr, int count) -> int {
+  auto ticket = [&](int* ctr, int count, int arrivals) -> int {
     __threadfence();
     if (!consumer_sync()) return -1;
     if (ct_all == 0) {
-      s_last = atomicAdd(ctr, 1) == count - 1;
+      s_last = atomicAdd(ctr, arrivals) + arrivals == count;
       __threadfence();
     }
     if (!consumer_sync()) return -1;
@@ -637,7 +640,16 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   // arrival completing a group folds it into the slot of its first member,
   // and the group completing the segment's count combines the group results,
   // so no CTA reads more than about max(K, nsl / K) partials.
-  auto publish_partial = [&](const Piece& p, int seg) -> bool {
+  // A CTA's consecutive pieces that count on the same counter (consecutive
+  // splits of one segment or group) arrive together: one fenced atomic adds
+  // them all, when the next piece counts elsewhere or the CTA is done.
+  struct Pending {
+    int* ctr;
+    int n, k, K, ng, r, h, seg;
+    int64_t dst;
+    Members mb;
+  };
+  auto pending_of = [&](const Piece& p, int seg) -> Pending {
     constexpr int kDirect = 16;
     const int64_t xseg = p.x0 - p.t0;  // global index of the segment's first tile
     const int w0 = worker_of(xseg, T, W);
@@ -647,42 +659,78 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     const bool dense = T >= W;
     const int nsl = dense ? w1 - w0 + 1 : p.n;
     const int me = dense ? p.s - w0 : p.t0;
-    Members mb;
-    mb.seg = seg;
-    mb.xseg = xseg;
-    mb.w0 = w0;
-    mb.dense = dense;
-    mb.i0 = 0;
-    mb.stride = 1;
-    int* ctr = a.seg_count + seg;
-    int n = nsl;
-    int64_t dst = -1;
-    int K = 1, ng = 1;
+    Pending q;
+    q.mb.seg = seg;
+    q.mb.xseg = xseg;
+    q.mb.w0 = w0;
+    q.mb.dense = dense;
+    q.mb.i0 = 0;
+    q.mb.stride = 1;
+    q.ctr = a.seg_count + seg;
+    q.n = nsl;
+    q.dst = -1;
+    q.K = 1;
+    q.ng = 1;
+    q.k = 1;
+    q.r = p.r;
+    q.h = p.h;
+    q.seg = seg;
     if (nsl > kDirect) {
-      K = static_cast<int>(sqrtf(static_cast<float>(nsl)));
+      int K = static_cast<int>(sqrtf(static_cast<float>(nsl)));
       while (K * K < nsl) ++K;
-      ng = (nsl + K - 1) / K;
+      q.K = K;
+      q.ng = (nsl + K - 1) / K;
       const int gi = me / K;
-      mb.i0 = gi * K;
-      n = min(K, nsl - mb.i0);
-      dst = seg + (dense ? w0 + mb.i0 : worker_of(xseg + mb.i0, T, W));
-      ctr = a.group_count + dst;
+      q.mb.i0 = gi * K;
+      q.n = min(K, nsl - q.mb.i0);
+      q.dst = seg + (dense ? w0 + q.mb.i0 : worker_of(xseg + q.mb.i0, T, W));
+      q.ctr = a.group_count + q.dst;
     }
+    return q;
+  };
+  // the pending arrivals: ticket, and the combines they complete
+  auto flush = [&](Pending q) -> bool {
+    int arrivals = q.k;
     for (;;) {
-      const int last = ticket(ctr, n);
+      const int last = ticket(q.ctr, q.n, arrivals);
       if (last < 0) return false;
       if (last == 0) return true;
-      if (!combine(mb, n, p.r, p.h, dst)) return false;
-      if (ct_all == 0) *ctr = 0;  // ready for the next call
-      if (dst < 0) return true;
+      if (!combine(q.mb, q.n, q.r, q.h, q.dst)) return false;
+      if (ct_all == 0) *q.ctr = 0;  // ready for the next call
+      if (q.dst < 0) return true;
       // the group is folded into the slot of its first member: on to the
       // segment's count of groups
-      ctr = a.seg_count + seg;
-      n = ng;
-      dst = -1;
-      mb.i0 = 0;
-      mb.stride = K;
+      q.ctr = a.seg_count + q.seg;
+      q.n = q.ng;
+      q.dst = -1;
+      q.mb.i0 = 0;
+      q.mb.stride = q.K;
+      arrivals = 1;
     }
+  };
+  // The pending arrivals live in shared memory (the same for every consumer
+  // thread): the piece that opened them and their count.  Consumer thread 0
+  // updates them only after a barrier that every reader has passed.
+  auto publish_partial = [&](const Piece& p, int seg) -> bool {
+    const int pk = s_pend_k;
+    const bool same = pk > 0 && pending_of(s_pend_piece, s_pend_seg).ctr == pending_of(p, seg).ctr;
+    if (pk > 0 && !same) {
+      Pending q = pending_of(s_pend_piece, s_pend_seg);
+      q.k = pk;
+      if (!flush(q)) return false;  // its barriers follow every thread's reads above
+    } else if (!consumer_sync()) {
+      return false;
+    }
+    if (ct_all == 0) {
+      if (same) {
+        s_pend_k = pk + 1;
+      } else {
+        s_pend_piece = p;
+        s_pend_seg = seg;
+        s_pend_k = 1;
+      }
+    }
+    return true;
   };
 
   zero_dead_rows(ct_all, kConsumerWarps * 32);
@@ -1027,39 +1075,62 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     }
     const int seg = p.r * a.Hkv + p.h;
     const bool whole = p.t0 == 0 && p.t1 == p.n;
-    const int ct = ct_all;
     int anyfault = 0;
 #pragma unroll
     for (int k = 0; k < nslots; ++k) anyfault |= s_wfault[k];
-    for (int idx = ct; idx < a.G * kDim; idx += kConsumerWarps * 32) {
-      const int hd = idx >> 7;
-      const int d = idx & (kDim - 1);
-      float M = kNegInf;
+    {
+      // 16 threads per head, 8 consecutive dims each: the slots' weights for
+      // the head, then two float4 of each slot
+      const int hd = ct_all >> 4;
+      const int d0 = (ct_all & 15) * 8;
+      if (hd < a.G) {
+        float mk[nslots];
+        float M = kNegInf;
 #pragma unroll
-      for (int k = 0; k < nslots; ++k) M = fmaxf(M, s_m[k * kGroupMax + hd]);
-      const bool dead = anyfault || M == kNegInf;
-      float wsum = 0.f, acc = 0.f;
+        for (int k = 0; k < nslots; ++k) {
+          mk[k] = s_m[k * kGroupMax + hd];
+          M = fmaxf(M, mk[k]);
+        }
+        const bool dead = anyfault || M == kNegInf;
+        float wsum = 0.f;
+        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
 #pragma unroll
-      for (int k = 0; k < nslots; ++k) {
-        const float mk = s_m[k * kGroupMax + hd];
-        const float f = mk == kNegInf ? 0.f : fast_exp2(mk - M);
-        wsum = fmaf(s_l[k * kGroupMax + hd], f, wsum);
-        acc = fmaf(s_mo[(k * kGroupMax + hd) * kMergeStride + d], f, acc);
-      }
-      if (whole) {
-        const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
-        a.out[row * kDim + d] = dead ? 0.f : acc * vmul / wsum;
-        if (d == 0 && a.lse != nullptr) a.lse[row] = dead ? kNegInf : (M + __log2f(wsum)) * kLn2;
-      } else {
-        const int64_t slot = static_cast<int64_t>(seg) + p.s;
-        a.part_o[(slot * a.G + hd) * kDim + d] = acc * vmul;
-        if (d == 0) a.part_ml[slot * a.G + hd] = dead ? make_float2(kNegInf, -1.f) : make_float2(M, wsum);
+        for (int k = 0; k < nslots; ++k) {
+          const float f = mk[k] == kNegInf ? 0.f : fast_exp2(mk[k] - M);
+          wsum = fmaf(s_l[k * kGroupMax + hd], f, wsum);
+          const float4* src = reinterpret_cast<const float4*>(s_mo + (k * kGroupMax + hd) * kMergeStride + d0);
+          const float4 x0 = src[0], x1 = src[1];
+          v0 = make_float4(fmaf(x0.x, f, v0.x), fmaf(x0.y, f, v0.y), fmaf(x0.z, f, v0.z), fmaf(x0.w, f, v0.w));
+          v1 = make_float4(fmaf(x1.x, f, v1.x), fmaf(x1.y, f, v1.y), fmaf(x1.z, f, v1.z), fmaf(x1.w, f, v1.w));
+        }
+        float4* dst;
+        float sc;
+        if (whole) {
+          const int64_t row = static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + hd;
+          dst = reinterpret_cast<float4*>(a.out + row * kDim + d0);
+          sc = dead ? 0.f : vmul / wsum;
+          if (d0 == 0 && a.lse != nullptr) a.lse[row] = dead ? kNegInf : (M + __log2f(wsum)) * kLn2;
+        } else {
+          const int64_t slot = static_cast<int64_t>(seg) + p.s;
+          dst = reinterpret_cast<float4*>(a.part_o + (slot * a.G + hd) * kDim + d0);
+          sc = vmul;
+          if (d0 == 0) a.part_ml[slot * a.G + hd] = dead ? make_float2(kNegInf, -1.f) : make_float2(M, wsum);
+        }
+        dst[0] = make_float4(v0.x * sc, v0.y * sc, v0.z * sc, v0.w * sc);
+        dst[1] = make_float4(v1.x * sc, v1.y * sc, v1.z * sc, v1.w * sc);
       }
     }
     if (!whole && !publish_partial(p, seg)) break;
     __syncwarp();
     if (lane == 0) mbar_arrive(merge_free);
     ++piece_idx;
+  }
+  // the last arrivals of this CTA (its shared-memory merge buffers are free:
+  // no piece follows)
+  if (ok && consumer_sync() && s_pend_k > 0) {
+    Pending q = pending_of(s_pend_piece, s_pend_seg);
+    q.k = s_pend_k;
+    flush(q);
   }
 }
 
@@ -1187,7 +1258,7 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
   if (B == 0) return FPK_OK;
   if (!q || !kv_pool || !page_table || !seq_lens || !out || !workspace) return FPK_EINVAL;
   if (kFp8 && (!k_scale || !v_scale)) return FPK_EINVAL;
-  if (!aligned16(q) || !aligned16(kv_pool) ||
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return FPK_EINVAL;
   int dev = 0;

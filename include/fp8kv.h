@@ -291,7 +291,7 @@ size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  *   q         : bf16 [B][Hq][D]
  *   abort_mask: uint8 [B] from fpk_page_tags_validate, or NULL (no-op tracker:
  *               no tag check)
- *   out       : float [B][Hq][D];  lse: float [B][Hq], nullable
+ *   out       : float [B][Hq][D], 16-byte aligned;  lse: float [B][Hq], nullable
  *   workspace : >= fpk_decode_workspace_bytes(...) bytes, 256-byte aligned,
  *               owned by the caller.  Zero it ONCE after allocating: it holds
  *               arrival counters that every call leaves at zero
