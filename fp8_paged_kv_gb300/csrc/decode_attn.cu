@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   __shared__ int s_last;
   __shared__ Piece s_pend_piece;  // the pending arrivals of split pieces (see publish_partial)
   __shared__ int s_pend_seg, s_pend_k;
+  __shared__ int* s_pend_ctr;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -712,8 +713,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   // thread): the piece that opened them and their count.  Consumer thread 0
   // updates them only after a barrier that every reader has passed.
   auto publish_partial = [&](const Piece& p, int seg) -> bool {
+    int* const ctr = pending_of(p, seg).ctr;
     const int pk = s_pend_k;
-    const bool same = pk > 0 && pending_of(s_pend_piece, s_pend_seg).ctr == pending_of(p, seg).ctr;
+    const bool same = pk > 0 && s_pend_ctr == ctr;
     if (pk > 0 && !same) {
       Pending q = pending_of(s_pend_piece, s_pend_seg);
       q.k = pk;
@@ -727,6 +729,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       } else {
         s_pend_piece = p;
         s_pend_seg = seg;
+        s_pend_ctr = ctr;
         s_pend_k = 1;
       }
     }

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from fp8_paged_kv_gb300 import fpk_decode_workspace_bytes
+from fp8_paged_kv_gb300 import FpkError, fpk_decode_workspace_bytes
 from fp8_paged_kv_gb300.pool import DecodePool, to_device
 from tests.gpu_helpers import assert_attention_close, oracle_attention, oracle_pools
 from workloads import b32_8k, b64_var, custom, long128k, rng_for, tiny
@@ -118,6 +118,16 @@ def test_repeated_launches_bit_identical(case):
         assert torch.equal(pool.out.view(torch.int32), first[0].view(torch.int32))
         assert torch.equal(pool.lse.view(torch.int32), first[1].view(torch.int32))
     assert pool.workspace[:4].view(torch.int32).item() == 0
+
+
+def test_rejects_misaligned_output():
+    wl = custom(88, B=2, Hq=8, Hkv=2, ps=16, prompt_lens=[40, 9], steps=0)
+    pool = DecodePool(wl, fp8=True, device=DEV)
+    pool.prefill()
+    buf = torch.empty(pool.out.numel() + 1, dtype=torch.float32, device=DEV)
+    pool.out = buf[1:].view(pool.out.shape)              # 4 bytes past a 16-byte boundary
+    with pytest.raises(FpkError):
+        pool.attend()
 
 
 def test_split_invariance():
