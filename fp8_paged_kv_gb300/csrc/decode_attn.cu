@@ -18,23 +18,26 @@
 //   cp.async.bulk (TMA) copy of one tile's K block [16 tok][128] and V block
 //   [128][16 tok] -- adjacent in the pool layout, so one copy of 4 KiB (FP8),
 //   or 8 KiB for two adjacent tiles of one page -- into a ring of shared-memory
-//   stages completing on mbarriers, with an L2 evict-first hint.  Page ids
+//   stages completing on mbarriers, with an L2 evict-first hint.  The FP8
+//   kernel comes with an 8-stage and a 12-stage ring; the deeper one is used
+//   while the grid's copies in flight stay within a budget.  Page ids
 //   outside the pool are never dereferenced.
 // * Math.  Consumer warps take ring stages round-robin.  With the GQA group on
 //   the N side of the tensor-core tile, S^T = K Q^T and O^T = V^T P^T are
 //   m16n8k16 MMAs; e4m3 codes convert exactly to f16 in registers (the query
-//   gets a per-head power-of-two prescale into f16 range), P is transposed
-//   from accumulator to operand layout with movmatrix, softmax is online in
-//   the log2 domain with warp-shuffle reductions.  The dims of each 16-wide
+//   gets a per-head power-of-two prescale into f16 range), P = hi + lo is
+//   transposed from accumulator to operand layout with movmatrix, softmax is
+//   online in the log2 domain with warp-shuffle reductions.  The dims of each 16-wide
 //   k-step and the tokens of each tile are visited in a fixed permuted order
 //   (the same on both operands), so every operand fragment is a contiguous
 //   4-byte run of shared memory.
 // * Merge.  At the end of each segment piece the consumer warps merge their
 //   (m, l, O) in shared memory; a CTA that owns a whole segment writes the
-//   final output, otherwise it writes a partial and takes an arrival ticket;
-//   the warp that completes a segment's count merges its partials by
-//   log-sum-exp in two branch-free passes (one launch per call; nothing ever
-//   waits on another CTA).
+//   final output, otherwise it writes a partial and counts an arrival (its
+//   consecutive arrivals on one counter in one ticket); the CTA whose
+//   arrivals complete a segment's count merges its partials by log-sum-exp,
+//   in two levels above 16 partials (one launch per call; nothing ever waits
+//   on another CTA).
 // * Safety.  Every wait is bounded (status word in the workspace); no barrier
 //   without a timeout is used after the prologue.
 #include <atomic>
