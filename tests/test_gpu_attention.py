@@ -49,7 +49,7 @@ def _run_case(wl, fp8, num_splits, abort=None, use_mask=True, pt_override=None):
 
 
 @pytest.mark.parametrize("fp8", [True, False])
-@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("ps", [16, 32, 64, 128, 256])
 def test_small_ragged(fp8, G, ps):
     Hkv = 2
