@@ -61,6 +61,17 @@ def test_small_ragged(fp8, G, ps):
 
 
 @pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("Hkv,G", [(1, 8), (1, 1), (16, 4), (32, 2)])
+def test_kv_head_counts(fp8, Hkv, G):
+    # one kv head (multi-query) up to 32 of them
+    lens = [0, 5, 16, 130, 700, 33]
+    wl = custom(90 + Hkv + G, B=len(lens), Hq=G * Hkv, Hkv=Hkv, ps=16, prompt_lens=lens, steps=0,
+                sigma=1.2, outlier_frac=0.02)
+    out, lse, ro, rl = _run_case(wl, fp8, num_splits=0)
+    assert_attention_close(out, lse, ro, rl, f"fp8={fp8} Hkv={Hkv} G={G}")
+
+
+@pytest.mark.parametrize("fp8", [True, False])
 @pytest.mark.parametrize("num_splits", [1, 2, 5, 37, 61, 200, 300, 4096])
 def test_split_counts(fp8, num_splits):
     lens = [700, 33, 0, 1025, 64, 5]
