@@ -33,6 +33,7 @@ _SZ = ctypes.c_size_t
 # name -> (restype, argtypes); mirrors include/fp8kv.h
 SIGNATURES = {
     "fpk_version": (ctypes.c_int, []),
+    "fpk_selftest_bounded_wait": (ctypes.c_int, [_P, _P, _P]),
     "fpk_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "fpk_kv_append_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P,
                                          _I32, _I32, _I32, _I32, _I32, _P]),
@@ -331,6 +332,14 @@ def fpk_decode_status(workspace, stream=None) -> int:
     _check(load_library().fpk_decode_status(_ptr(workspace, _U8, "workspace"), ctypes.byref(v),
                                             _stream(stream)), "fpk_decode_status")
     return int(v.value)
+
+
+def fpk_selftest_bounded_wait(status, elapsed_ns, stream=None):
+    """One CTA waits on an mbarrier nothing arrives on; the bounded wait gives up
+    after its limit and reports it in status[0] (elapsed time in elapsed_ns[0])."""
+    _check(load_library().fpk_selftest_bounded_wait(_ptr(status, torch.int32, "status"),
+                                                    _ptr(elapsed_ns, torch.int64, "elapsed_ns"),
+                                                    _stream(stream)), "fpk_selftest_bounded_wait")
 
 
 # ---------------------------------------------------------------- weight GEMV

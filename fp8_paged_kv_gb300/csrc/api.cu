@@ -44,7 +44,31 @@ int resident_grid(const void* kernel, int threads, size_t dyn_smem, int64_t want
   return static_cast<int>(want < cap ? want : cap);
 }
 
+namespace {
+// Self-test of the bounded wait every kernel uses: one CTA waits on an
+// mbarrier that nothing arrives on.  The wait gives up after kWaitLimitNs,
+// sets kStatusWaitTimeout in *status and returns; the kernel records how long
+// the wait took.
+__global__ void bounded_wait_selftest_kernel(uint32_t* status, unsigned long long* elapsed_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const uint64_t t0 = global_timer_ns();
+  const bool got = mbar_wait(smem_addr(&bar), 0, status);
+  if (threadIdx.x == 0) *elapsed_ns = got ? 0ull : global_timer_ns() - t0;
+}
+}  // namespace
+
 }  // namespace fpk
+
+extern "C" int fpk_selftest_bounded_wait(uint32_t* status, unsigned long long* elapsed_ns, void* stream) {
+  if (!status || !elapsed_ns) return FPK_EINVAL;
+  fpk::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, elapsed_ns);
+  return fpk::checked_launch_status();
+}
 
 extern "C" int fpk_version(void) { return 100; }
 

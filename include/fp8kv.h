@@ -397,6 +397,17 @@ int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* kv_pool,
  */
 int fpk_decode_status(const void* workspace, int32_t* status, void* stream);
 
+/*
+ * Self-test of the bounded waits (the failure report every kernel relies on,
+ * not a step of the path).  Launches one CTA that waits on an mbarrier nothing
+ * arrives on: the wait gives up after its time limit (2 s), ORs 1 into *status
+ * (the same bit the attention kernel sets in its workspace status word) and
+ * the kernel exits; *elapsed_ns receives the time the wait took.  The context
+ * stays usable.
+ *   status    : uint32 [1], device; elapsed_ns: uint64 [1], device
+ */
+int fpk_selftest_bounded_wait(uint32_t* status, unsigned long long* elapsed_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,7 +14,7 @@ import oracle
 from fp8_paged_kv_gb300 import FpkError, fpk_decode_step_fp8
 from fp8_paged_kv_gb300.pool import DecodePool, to_device
 from tests.gpu_helpers import assert_attention_close, oracle_attention, oracle_pools
-from workloads import custom
+from workloads import custom, tiny
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -131,3 +131,24 @@ def test_rejected_step_launches_nothing():
                             num_pages=wl.num_pages, sm_scale=wl.sm_scale)
     torch.cuda.synchronize()
     assert np.array_equal(a.pool_bytes(), before)   # the write did not run either
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """A wait that nothing completes ends after its limit with the timeout bit
+    set, and the context stays usable (a full decode step runs after it)."""
+    from fp8_paged_kv_gb300 import fpk_selftest_bounded_wait
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    elapsed = torch.zeros(1, dtype=torch.int64, device=DEV)
+    fpk_selftest_bounded_wait(status, elapsed)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    assert 1.9e9 <= int(elapsed.item()) <= 4e9
+    wl = tiny()
+    pool = DecodePool(wl, fp8=True, device=DEV)
+    pool.prefill()
+    pool.set_step(0)
+    pool.count_aborts = False
+    pool.step(validate=True)
+    torch.cuda.synchronize()
+    assert pool.workspace[:4].view(torch.int32).item() == 0
+    assert list(pool.abort_mask.cpu().numpy()) == [0, 1]
