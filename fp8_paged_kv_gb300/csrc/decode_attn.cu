@@ -54,6 +54,24 @@ constexpr int kGroupMax = 8;     // query heads per kv head (N of the MMA tile)
 constexpr int kMergeStride = 132;  // floats per head row of the merge buffer
 constexpr int kMergeBars = 6;      // merge_free, cbar, the three rounds of the two-slot merge, the four-slot one
 constexpr int64_t kInflightBudget = 26ll << 20;  // bytes of ring stages over the grid (see Cfg)
+// The automatic split count: one wave of CTAs, but no more than 16 splits per
+// (request, kv head) segment -- small batches then keep the one-level combine
+// and CTAs with enough tiles to cover their start-up.
+constexpr int kAutoSplitsPerSegment = 16;
+
+// The automatic split count of a batch whose segments all have one length
+// (seen on the device, from the context lengths): one whole segment per CTA
+// when the segments fill between 3/4 of the CTAs and all of them; with fewer
+// segments, the same number of splits for each (as many as the CTAs allow,
+// at most kAutoSplitsPerSegment), which puts every split boundary on a
+// segment boundary -- no split straddles two segments.  0: keep the count.
+__host__ __device__ __forceinline__ int64_t uniform_auto_splits(int64_t segs, int64_t nctas) {
+  if (segs <= 0 || segs > nctas) return 0;
+  if (4 * segs >= 3 * nctas) return segs;
+  int64_t m = nctas / segs;
+  if (m > kAutoSplitsPerSegment) m = kAutoSplitsPerSegment;
+  return segs * m;
+}
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 static_assert(kConsumerWarps * 32 == 128, "the split-segment combine gives each consumer thread one of the 128 dims");
@@ -285,13 +303,15 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   const int64_t T = total * a.Hkv;
   const int nctas = static_cast<int>(gridDim.x);
   // Split count.  With the automatic count, a batch whose (request, kv head)
-  // segments all have the same length and number between 3/4 of the CTAs and
-  // all of them runs one whole segment per CTA: no split partials, no
-  // cross-CTA combine (it costs less than the idle quarter of the CTAs).
+  // segments all have the same length takes uniform_auto_splits: a batch of
+  // between 3/4 of the CTAs and all of them runs one whole segment per CTA
+  // (no split partials, no cross-CTA combine: that costs less than the idle
+  // quarter of the CTAs); a smaller one gets an equal number of splits per
+  // segment, aligned to the segments.
   int W = a.W;
   if (a.auto_split && nz_all > 0 && tmin_all == tmax_all) {
-    const int64_t segs = static_cast<int64_t>(nz_all) * a.Hkv;
-    if (4 * segs >= 3 * static_cast<int64_t>(nctas) && segs <= nctas) W = static_cast<int>(segs);
+    const int64_t u = uniform_auto_splits(static_cast<int64_t>(nz_all) * a.Hkv, nctas);
+    if (u > 0) W = static_cast<int>(u);
   }
   // this CTA runs splits [s0, s1) one after another: tiles [b0, b1)
   const int64_t s0 = static_cast<int64_t>(w) * W / nctas;
@@ -1181,10 +1201,6 @@ WsLayout layout(int64_t B, int64_t Hkv, int64_t G, int64_t W) {
   return l;
 }
 
-// The automatic split count: one wave of CTAs, but no more than 16 splits per
-// (request, kv head) segment -- small batches then keep the one-level combine
-// and CTAs with enough tiles to cover their start-up.
-constexpr int kAutoSplitsPerSegment = 16;
 int auto_splits(int wave, int B, int Hkv) {
   const int64_t cap = static_cast<int64_t>(kAutoSplitsPerSegment) * B * Hkv;
   return cap < wave ? static_cast<int>(cap) : wave;
@@ -1213,15 +1229,17 @@ enum class AttnLaunch { kPlain, kCheckOnly, kAfterStepWrite };
 
 // The deep-ring FP8 variant pays when the CTAs that will have work keep no
 // more than kInflightBudget of stages in flight: a grid of at most W CTAs, or
-// the whole-segment mode, which the kernel takes for a uniform batch of
-// between 3/4 of the CTAs and all of them segments (the host cannot see the
-// context lengths; if they turn out uneven, the deep variant runs with its
-// shallow ring).  It must also fit as many CTAs per SM as the shallow one.
+// the split count the kernel takes for a uniform batch (uniform_auto_splits;
+// the host cannot see the context lengths and assumes every request holds
+// tokens -- if they turn out uneven, the deep variant runs with its shallow
+// ring).  It must also fit as many CTAs per SM as the shallow one.
 bool deep_ring(int dev, int W, int ctas, int B, int Hkv, bool auto_split) {
   using D = Cfg<true, true>;
-  const int64_t segs = static_cast<int64_t>(B) * Hkv;
   int64_t active = W < ctas ? W : ctas;
-  if (auto_split && 4 * segs >= 3 * static_cast<int64_t>(ctas) && segs <= ctas) active = segs;
+  if (auto_split) {
+    const int64_t u = uniform_auto_splits(static_cast<int64_t>(B) * Hkv, ctas);
+    if (u > 0) active = u;
+  }
   if (active * D::kStages * D::kStageBytes > kInflightBudget) return false;
   const int deep = prepare_kernel<true, true>(dev);
   return deep > 0 && deep >= prepare_kernel<true, false>(dev);

@@ -96,6 +96,19 @@ def test_uniform_batch_one_segment_per_cta(fp8, abort_one):
 
 
 @pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("lens", [[700] * 4, [0, 333, 333, 0, 333], [160] * 20, [1] * 3])
+def test_uniform_small_batch_segment_aligned_splits(fp8, lens):
+    # equal context lengths (empty requests aside) and fewer segments than 3/4
+    # of the CTAs: the automatic count gives every segment the same number of
+    # splits, all split boundaries on segment boundaries (one whole segment
+    # per CTA once the segments fill half the CTAs)
+    wl = custom(89 + len(lens), B=len(lens), Hq=64, Hkv=8, ps=16, prompt_lens=lens, steps=0,
+                sigma=1.0, outlier_frac=0.01)
+    out, lse, ro, rl = _run_case(wl, fp8, 0)
+    assert_attention_close(out, lse, ro, rl, f"uniform small fp8={fp8} lens={lens[:3]}")
+
+
+@pytest.mark.parametrize("fp8", [True, False])
 def test_uneven_batch_of_whole_segment_size(fp8):
     # 30 x 8 segments, as above, but of uneven lengths: the host launches the
     # deep-ring FP8 variant for a batch that may run one whole segment per CTA;
