@@ -304,7 +304,10 @@ size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  *               divided into (balanced by tile count across all requests and
  *               kv heads); each split's partial enters the log-sum-exp
  *               combine.  0 = automatic: one wave of CTAs, at most 16 per
- *               (request, kv head).  With equal
+ *               (request, kv head); when every non-empty request has the
+ *               same length, one whole (request, kv head) per CTA if they
+ *               fill 3/4 of a wave or more, else an equal number of splits
+ *               per (request, kv head) (at most 16).  With equal
  *               context lengths, num_splits = S * B * Hkv gives exactly S
  *               splits per (request, kv head).  At most one wave of CTAs is
  *               launched; beyond that a CTA runs several splits in turn.
