@@ -154,6 +154,16 @@ def test_rejects_misaligned_output():
         pool.attend()
 
 
+@pytest.mark.parametrize("fp8", [True, False])
+def test_thousands_of_short_requests(fp8):
+    # 3000 requests of 0..70 tokens: ~20 segments per CTA, most of them whole,
+    # the rest cut between CTAs (partials, batched arrivals, combines)
+    lens = list(rng_for(91, "lens").integers(0, 71, size=3000))
+    wl = custom(91, B=3000, Hq=8, Hkv=2, ps=16, prompt_lens=lens, steps=0)
+    out, lse, ro, rl = _run_case(wl, fp8, 0)
+    assert_attention_close(out, lse, ro, rl, f"3000 short fp8={fp8}")
+
+
 def test_split_invariance():
     lens = [3000, 1, 900]
     wl = custom(80, B=3, Hq=32, Hkv=4, ps=32, prompt_lens=lens, steps=0)
