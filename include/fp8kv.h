@@ -307,7 +307,11 @@ size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  *               (request, kv head); when every non-empty request has the
  *               same length, one whole (request, kv head) per CTA if they
  *               fill 3/4 of a wave or more, else an equal number of splits
- *               per (request, kv head) (at most 16).  With equal
+ *               per (request, kv head) (at most 16); when lengths
+ *               differ and the non-empty (request, kv head) pairs number at
+ *               most a third of a wave, each is cut into splits of one
+ *               common tile count c = ceil(tiles / (wave - pairs)) (its last
+ *               split shorter), one split per CTA.  With equal
  *               context lengths, num_splits = S * B * Hkv gives exactly S
  *               splits per (request, kv head).  At most one wave of CTAs is
  *               launched; beyond that a CTA runs several splits in turn.

@@ -109,6 +109,25 @@ def test_uniform_small_batch_segment_aligned_splits(fp8, lens):
 
 
 @pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("lens,abort_at", [([3000, 80], None), ([1, 2500, 17, 1111, 0], 3),
+                                           ([900, 16, 17, 31, 33, 1500, 700, 2, 1200], None),
+                                           ([4097, 4096, 4095, 4094, 4093, 4092, 4091, 4090, 4089, 4088, 4087, 4086], 0)])
+def test_mixed_small_batch_segment_aligned_splits(fp8, lens, abort_at):
+    # unequal context lengths and at most a third as many segments as CTAs:
+    # the automatic count cuts every segment into splits of one common tile
+    # count (the last one of a segment shorter), one split per CTA, so no
+    # split straddles two segments and each CTA merges into one segment only
+    wl = custom(97 + len(lens), B=len(lens), Hq=64, Hkv=8, ps=16, prompt_lens=lens, steps=0,
+                sigma=1.0, outlier_frac=0.01)
+    abort = None
+    if abort_at is not None:
+        abort = np.zeros(wl.B, np.uint8)
+        abort[abort_at] = 1
+    out, lse, ro, rl = _run_case(wl, fp8, 0, abort=abort, use_mask=abort is not None)
+    assert_attention_close(out, lse, ro, rl, f"mixed small fp8={fp8} lens={lens[:3]}")
+
+
+@pytest.mark.parametrize("fp8", [True, False])
 def test_uneven_batch_of_whole_segment_size(fp8):
     # 30 x 8 segments, as above, but of uneven lengths: the host launches the
     # deep-ring FP8 variant for a batch that may run one whole segment per CTA;
