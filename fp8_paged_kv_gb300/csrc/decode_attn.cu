@@ -825,6 +825,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   zero_dead_rows(ct_all, kConsumerWarps * 32);
   int ab_r = -1;  // request whose abort flag is cached
   bool ab = false;
+  int q_r = -1, q_h = -1;  // segment whose query fragments qf hold
+  uint32_t qf[8][2];
+  float mult_own = 0.f;
   while (ok && next_piece(cur, a, T, W, p)) {
     if (p.r != ab_r) {
       ab_r = p.r;
@@ -832,10 +835,11 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     }
     const int ntiles = p.t1 - p.t0;
     const int L = __ldg(a.seq_lens + p.r);
-    // ---- query fragments (B operand of S^T = K Q^T), heads of this kv group
-    uint32_t qf[8][2];
-    float mult_own = 0.f;
-    {
+    // ---- query fragments (B operand of S^T = K Q^T), heads of this kv group;
+    // kept from the previous piece when it was of the same segment
+    if (p.r != q_r || p.h != q_h) {
+      q_r = p.r;
+      q_h = p.h;
       const bool has = g < a.G;
       const uint16_t* qrow = a.q + (static_cast<int64_t>(p.r) * a.Hq + p.h * a.G + (has ? g : 0)) * kDim;
       if (kFp8) {
