@@ -149,18 +149,58 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# the sources compiled into the attention kernel's translation unit
+KERNEL_SOURCES = ("decode_attn.cu", "common.cuh", "step_ops.cuh", "quant.cuh")
+
+
+def _strip_comments(src: str) -> str:
+    """C/C++ source without comments, every run of whitespace made one space
+    (a comment marker inside a string or character literal is not a comment)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_source_digest(read=None) -> str:
+    """sha256 prefix of the attention kernel's sources with comments and
+    whitespace removed: it changes when the compiled code can, not when a
+    comment does.  read(name) -> text overrides where the files come from."""
+    import hashlib
+    csrc = os.path.join(ROOT, "fp8_paged_kv_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                return f.read()
+    body = "\n".join(_strip_comments(read(n)) for n in KERNEL_SOURCES)
+    return hashlib.sha256(body.encode("utf-8")).hexdigest()[:16]
+
+
 def read_profile_traffic(workload: str, tag: str = "fp8"):
     """Per-launch DRAM bytes (read + write) of the attention kernel from the committed
     ncu record, or None when there is none or the kernel source changed since."""
-    import hashlib
     p = os.path.join(ROOT, "profiles", f"paged_decode_attn_{tag}_{workload}.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    csrc = os.path.join(ROOT, "fp8_paged_kv_gb300", "csrc")
-    src = b"".join(open(os.path.join(csrc, n), "rb").read() for n in ("decode_attn.cu", "common.cuh"))
-    if hashlib.sha256(src).hexdigest()[:16] != d.get("source_sha256_16"):
+    if kernel_source_digest() != d.get("source_sha256_16"):
         return None
     return d.get("dram_bytes_per_launch")
 

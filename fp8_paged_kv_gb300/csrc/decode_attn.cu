@@ -13,7 +13,12 @@
 //   wave of CTAs by default), so variable context lengths cost no tail.  At
 //   most one wave of CTAs runs; with more splits than that a CTA takes
 //   consecutive splits in turn without draining its copy pipeline between
-//   them.  A CTA finds its start with a block scan over seq_lens.
+//   them, keeping its query fragments while the segment stays the same.  A
+//   CTA finds its start with a block scan over seq_lens.  With the automatic
+//   count, batches with few segments get split boundaries on segment
+//   boundaries instead: equal lengths give every segment the same number of
+//   splits (one whole segment per CTA once they fill 3/4 of a wave), unequal
+//   ones cut every segment into splits of one common size, one per CTA.
 // * Data movement.  Warp 0 is a producer: each of its lanes issues one
 //   cp.async.bulk (TMA) copy of one tile's K block [16 tok][128] and V block
 //   [128][16 tok] -- adjacent in the pool layout, so one copy of 4 KiB (FP8),
