@@ -525,6 +525,23 @@ def time_e2e(pool, steps: int, warmup: int):
     return ms, h2d, d2h
 
 
+class L2Flush:
+    """Evicts L2 before a timed launch: a 512 MB write, then a 512 MB read, so the
+    launch starts with a cold L2 that holds no dirty lines.  (After the write alone
+    ~126 MB of dirty lines are written back while the timed kernel runs, 9-14 us
+    on GB300, which no real decode step has: the kernels before attention mostly
+    read weights.)"""
+    NOTE = "flushed before every timed launch (512 MB write, then 512 MB read)"
+
+    def __init__(self, dev):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.sink = self.r.sum(dtype=torch.int64)
+
+
 def run_capacity(args, rank, world):
     """Admission at a fixed KV budget (one layer): how many 8192-token requests of
     the b32_8k shape (Hq=64, Hkv=8, D=128, page 16) fit in the pool with a BF16
@@ -544,7 +561,7 @@ def run_capacity(args, rank, world):
     ppr = L // ps
     g = torch.Generator(device=dev)
     g.manual_seed(7 + rank)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     s = torch.cuda.current_stream(dev)
     curves = {}
     with ClockSampler(local_rank()) as clk:
@@ -580,7 +597,7 @@ def run_capacity(args, rank, world):
                         fpk.fpk_paged_decode_attn_bf16(q, pool, pt, lens, None, out, lse, ws, **kw)
                 t = []
                 for i in range(3 + args.capacity_reps):
-                    flush.zero_()
+                    flush()
                     a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(s)
                     run()
@@ -604,7 +621,7 @@ def run_capacity(args, rank, world):
             "fp8_over_bf16_cap": f8["cap_requests"] / max(1, bf["cap_requests"]),
             "fp8_at_cap_over_bf16_at_cap_tokens_per_s":
                 f8["points"][-1]["tokens_per_s"] / bf["points"][-1]["tokens_per_s"],
-            "l2": "flushed (512 MB write) before every timed launch", "clocks": clk.summary()}
+            "l2": L2Flush.NOTE, "clocks": clk.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -633,7 +650,7 @@ def run_gemv(args, rank, world):
     fpk.fpk_w4_quantize(w, c4, s4)
     fpk.fpk_w8_quantize(w, c8, r8)
     del w
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     s = torch.cuda.current_stream(dev)
     peak, peak_kind = measured_peaks()
     pts = []
@@ -646,7 +663,7 @@ def run_gemv(args, rank, world):
                                      ("fp8", lambda: fpk.fpk_w8_gemv(x, c8, r8, y), N * K + N * 4)):
                 t = []
                 for i in range(3 + args.capacity_reps):
-                    flush.zero_()
+                    flush()
                     a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(s)
                     fn()
@@ -662,7 +679,7 @@ def run_gemv(args, rank, world):
             pts.append(row)
     line = {"mode": "gemv", "shape": f"N={N}, K={K}, random-init bf16 weights", "points": pts,
             "peak_gbs": peak, "peak_source": peak_kind,
-            "l2": "flushed (512 MB write) before every timed launch", "clocks": clk.summary()}
+            "l2": L2Flush.NOTE, "clocks": clk.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
