@@ -78,3 +78,51 @@ def test_no_oracle_in_the_product():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "fp8kv_oracle" not in text, f
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """Without the built library the binding raises; it has no fallback."""
+    import fp8_paged_kv_gb300 as fpk
+    monkeypatch.setattr(fpk, "_lib", None)
+    with pytest.raises(fpk.FpkError, match="no fallback"):
+        fpk.load_library(str(tmp_path / "absent.so"))
+
+
+def test_cpu_tensors_are_refused(lib):
+    """Every compute entry point refuses host tensors before calling the
+    library: there is no CPU path to fall back to."""
+    import torch
+
+    import fp8_paged_kv_gb300 as fpk
+    B, Hq, Hkv, D, ps, P = 2, 8, 2, 128, 16, 4
+    pool8 = torch.zeros(2 * P * Hkv * ps * D, dtype=torch.uint8)
+    pool16 = torch.zeros(2 * P * Hkv * ps * D, dtype=torch.bfloat16)
+    kv = torch.zeros(B, Hkv, D, dtype=torch.bfloat16)
+    q = torch.zeros(B, Hq, D, dtype=torch.bfloat16)
+    pt = torch.zeros(B, 2, dtype=torch.int32)
+    lens = torch.ones(B, dtype=torch.int32)
+    sc = torch.ones(1)
+    out, lse = torch.zeros(B, Hq, D), torch.zeros(B, Hq)
+    ws = torch.zeros(4096, dtype=torch.uint8)
+    tags, exp = torch.zeros(P, dtype=torch.int32), torch.zeros(B, 2, dtype=torch.int32)
+    mask = torch.zeros(B, dtype=torch.uint8)
+    geo = dict(Hkv=Hkv, page_size=ps, num_pages=P)
+    calls = {
+        "append_fp8": lambda: fpk.fpk_kv_append_fp8(kv, kv, pool8, sc, sc, pt, lens, D=D, **geo),
+        "append_bf16": lambda: fpk.fpk_kv_append_bf16(kv, kv, pool16, pt, lens, D=D, **geo),
+        "bump": lambda: fpk.fpk_page_tags_bump(tags, torch.zeros(1, dtype=torch.int32), num_pages=P),
+        "validate": lambda: fpk.fpk_page_tags_validate(pt, exp, lens, tags, mask, num_pages=P,
+                                                       page_size=ps),
+        "attn_fp8": lambda: fpk.fpk_paged_decode_attn_fp8(q, pool8, sc, sc, pt, lens, None, out, lse,
+                                                          ws, sm_scale=0.1, **geo),
+        "attn_bf16": lambda: fpk.fpk_paged_decode_attn_bf16(q, pool16, pt, lens, None, out, lse, ws,
+                                                            sm_scale=0.1, **geo),
+        "step_fp8": lambda: fpk.fpk_decode_step_fp8(kv, kv, pool8, sc, sc, pt, lens, tags, exp, mask,
+                                                    q, out, lse, ws, sm_scale=0.1, **geo),
+        "w4_gemv": lambda: fpk.fpk_w4_gemv(torch.zeros(1, 128, dtype=torch.bfloat16),
+                                           torch.zeros(64, dtype=torch.uint8),
+                                           torch.zeros(1, dtype=torch.bfloat16), torch.zeros(1, 1)),
+    }
+    for name, call in calls.items():
+        with pytest.raises(fpk.FpkError, match="CUDA"):
+            call()
