@@ -7,8 +7,8 @@
 // the request ("Cosa ha cambiato Cloudflare per Kimi e GLM" and "La sicurezza
 // della cache KV condivisa diventa una questione di produzione", remio.ai).
 // The check is its own batched kernel -- a pure gather-compare -- and is not
-// fused into attention (the same section: fusing it raced between GPU thread
-// groups).
+// fused into attention ("La sicurezza della cache KV condivisa...": fused, the
+// check could race between GPU thread groups).
 #include "step_ops.cuh"
 
 namespace fpk {

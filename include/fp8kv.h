@@ -224,8 +224,8 @@ int fpk_page_tags_bump(uint32_t* live_tags, const int32_t* pages, int32_t n, int
 /*
  * Batched page-tag validation, a separate pure gather-compare that runs before
  * attention (never fused into it: "La sicurezza della cache KV condivisa..."
- * says the check was kept out of the attention kernel because of races
- * between GPU thread groups).
+ * says the check was kept out of the attention kernel because GPU thread
+ * groups could have raced there).
  * For every request r, with P = ceil(seq_lens[r] / page_size) (0 if L <= 0):
  *   abort_mask[r] = 1 iff P > max_pages, or some i < P has page_table[r][i]
  *   outside [0, num_pages) or live_tags[page_table[r][i]] != expected_tags[r][i];
