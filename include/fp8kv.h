@@ -36,7 +36,8 @@
  * columns in each request's page table.
  *
  * Supported sizes: D == 128; page_size a multiple of 16 in [16, 256];
- * 1 <= G <= 8; B, Hkv >= 1.  Others return FPK_EUNSUPPORTED.
+ * 1 <= G <= 8.  Others return FPK_EUNSUPPORTED.  B == 0 is a no-op (FPK_OK);
+ * Hq or Hkv below 1 is FPK_EINVAL.
  *
  * KV pool layout (one pool per layer holding K and V; bytes per element: 1
  * for the e4m3 pool, 2 for the bf16 pool):

@@ -126,3 +126,47 @@ def test_cpu_tensors_are_refused(lib):
     for name, call in calls.items():
         with pytest.raises(fpk.FpkError, match="CUDA"):
             call()
+
+
+def test_attention_argument_errors_before_any_device_call():
+    """The attention entry points reject bad shapes, missing pointers and
+    misaligned buffers synchronously, before they ask for a device.  Every call
+    here returns at one of those checks (the pointers are never dereferenced);
+    the test is skipped where a device exists, so that a regression in the
+    order of the checks can never launch on the fake pointers."""
+    import torch
+
+    import fp8_paged_kv_gb300 as fpk
+    if torch.cuda.is_available():
+        pytest.skip("host-side checks only; run where no device is visible")
+    lib = fpk.load_library()
+    A = 1 << 20  # a 256-byte aligned fake address
+    OK, EINVAL, EUNSUP = fpk.FPK_OK, fpk.FPK_EINVAL, fpk.FPK_EUNSUPPORTED
+
+    def fp8(q=A, kv=A, ks=A, vs=A, pt=A, lens=A, out=A, ws=A, B=2, Hq=16, Hkv=2, D=128, ps=16,
+            num_pages=8, max_pages=4, splits=0):
+        return lib.fpk_paged_decode_attn_fp8(q, kv, ks, vs, pt, max_pages, lens, None, out, None, ws,
+                                             1 << 20, splits, 0.1, B, Hq, Hkv, D, ps, num_pages, None)
+
+    def bf16(q=A, kv=A, pt=A, lens=A, out=A, ws=A, B=2, Hq=16, Hkv=2, D=128, ps=16):
+        return lib.fpk_paged_decode_attn_bf16(q, kv, pt, 4, lens, None, out, None, ws, 1 << 20, 0, 0.1,
+                                              B, Hq, Hkv, D, ps, 8, None)
+
+    assert fp8(B=0, q=None, kv=None, out=None, ws=None) == OK        # nothing to do
+    assert fp8(Hq=15) == EINVAL                                     # Hq % Hkv != 0
+    assert fp8(Hkv=0) == EINVAL
+    assert fp8(B=-1) == EINVAL
+    assert fp8(splits=-1) == EINVAL
+    assert fp8(max_pages=-1) == EINVAL
+    assert fp8(D=64) == EUNSUP
+    assert fp8(Hq=32, Hkv=2) == EUNSUP                              # G = 16 > 8
+    assert fp8(ps=24) == EUNSUP and fp8(ps=512) == EUNSUP
+    for name in ("q", "kv", "ks", "vs", "pt", "lens", "out", "ws"):
+        assert fp8(**{name: None}) == EINVAL, name                   # required pointers
+    assert fp8(q=A + 2) == EINVAL                                   # q 16-byte aligned
+    assert fp8(kv=A + 8) == EINVAL
+    assert fp8(out=A + 4) == EINVAL                                 # out 16-byte aligned
+    assert fp8(ws=A + 16) == EINVAL                                 # workspace 256-byte aligned
+    assert bf16(Hq=15) == EINVAL and bf16(D=256) == EUNSUP
+    assert bf16(out=A + 4) == EINVAL and bf16(ws=None) == EINVAL
+    assert bf16(B=0, q=None) == OK
