@@ -170,3 +170,44 @@ def test_attention_argument_errors_before_any_device_call():
     assert bf16(Hq=15) == EINVAL and bf16(D=256) == EUNSUP
     assert bf16(out=A + 4) == EINVAL and bf16(ws=None) == EINVAL
     assert bf16(B=0, q=None) == OK
+
+
+def test_write_and_gemv_argument_errors_before_any_device_call():
+    """The same for the cache writes and the weight GEMV: every call below
+    returns at a host-side check (skipped where a device exists)."""
+    import torch
+
+    import fp8_paged_kv_gb300 as fpk
+    if torch.cuda.is_available():
+        pytest.skip("host-side checks only; run where no device is visible")
+    lib = fpk.load_library()
+    A = 1 << 20
+    OK, EINVAL, EUNSUP = fpk.FPK_OK, fpk.FPK_EINVAL, fpk.FPK_EUNSUPPORTED
+
+    def append(k=A, v=A, pool=A, ks=A, vs=A, pt=A, lens=A, B=2, Hkv=2, D=128, ps=16, num_pages=8,
+               max_pages=4):
+        return lib.fpk_kv_append_fp8(k, v, pool, ks, vs, pt, max_pages, lens, None, None, None,
+                                     B, Hkv, D, ps, num_pages, None)
+
+    def prefill(cu=A, n=32, B=2):
+        return lib.fpk_kv_prefill_fp8(A, A, cu, n, A, A, A, A, 4, None, None, None, B, 2, 128, 16, 8,
+                                      None)
+
+    assert append(B=0, k=None) == OK
+    assert append(Hkv=0) == EINVAL and append(B=-1) == EINVAL and append(num_pages=-1) == EINVAL
+    assert append(D=64) == EUNSUP and append(ps=8) == EUNSUP and append(ps=272) == EUNSUP
+    for name in ("k", "v", "pool", "ks", "vs", "pt", "lens"):
+        assert append(**{name: None}) == EINVAL, name
+    assert append(k=A + 2) == EINVAL and append(v=A + 8) == EINVAL and append(pool=A + 1) == EINVAL
+    assert prefill(n=0) == OK and prefill(n=-1) == EINVAL and prefill(cu=None) == EINVAL
+
+    def w4(x=A, codes=A, scales=A, y=A, B=1, N=64, K=256):
+        return lib.fpk_w4_gemv(x, codes, scales, y, B, N, K, None)
+
+    assert w4(B=0) == OK and w4(N=0) == OK
+    assert w4(B=17) == EUNSUP and w4(N=24) == EUNSUP and w4(K=200) == EUNSUP
+    assert w4(B=-1) == EINVAL and w4(N=-16) == EINVAL
+    for name in ("x", "codes", "scales", "y"):
+        assert w4(**{name: None}) == EINVAL, name
+    assert w4(x=A + 4) == EINVAL and w4(codes=A + 8) == EINVAL
+    assert lib.fpk_w8_gemv(A, A, None, A, 1, 64, 256, None) == EINVAL   # row scales required
