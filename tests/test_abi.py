@@ -4,6 +4,7 @@ call is made here: this runs on hosts without a GPU)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -211,3 +212,24 @@ def test_write_and_gemv_argument_errors_before_any_device_call():
         assert w4(**{name: None}) == EINVAL, name
     assert w4(x=A + 4) == EINVAL and w4(codes=A + 8) == EINVAL
     assert lib.fpk_w8_gemv(A, A, None, A, 1, 64, 256, None) == EINVAL   # row scales required
+
+
+def test_header_is_plain_c(tmp_path, lib):
+    """include/fp8kv.h compiles as strict C99 and a C program links against
+    the library and calls its host-only entry points."""
+    import shutil
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    from fp8_paged_kv_gb300 import LIB_PATH
+    src = tmp_path / "abi.c"
+    src.write_text('#include "fp8kv.h"\n#include <stdio.h>\n'
+                   'int main(void) { printf("%d %s\\n", fpk_version(), fpk_status_str(FPK_ENOSPC));\n'
+                   '  return 0; }\n')
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I",
+                    os.path.join(ROOT, "include"), str(src), "-L", libdir, "-lfp8kv",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split(" ", 1)
+    assert int(out[0]) >= 100 and out[1].strip()
