@@ -233,3 +233,16 @@ def test_header_is_plain_c(tmp_path, lib):
                     f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True, capture_output=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split(" ", 1)
     assert int(out[0]) >= 100 and out[1].strip()
+
+
+def test_library_exports_nothing_undeclared(lib):
+    """Every fpk_ symbol the library exports is declared in the header."""
+    import shutil
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("no nm")
+    from fp8_paged_kv_gb300 import LIB_PATH
+    out = subprocess.run([nm, "-D", "--defined-only", LIB_PATH], check=True, capture_output=True,
+                         text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.split() and ln.split()[-1].startswith("fpk_")}
+    assert exported == set(declared_symbols())
