@@ -1,7 +1,8 @@
 """CPU oracle of the FP8 paged-KV decode path (test infrastructure only).
 
 Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
-baseline leg import this package.  The product library never does, and this
+baseline leg and reference arm (``bench.py --impl reference``) import this
+package.  The product library never does, and this
 package imports nothing from it: the two share no code.
 
 The arithmetic lives in ``fp8kv_oracle.c`` (plain C, fp64); this module only

@@ -3,7 +3,7 @@
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, calls or
  * includes this file; only the test suite, the package entry's smoke check and
- * the CPU-baseline leg of the benchmark load it.  It shares no header, helper,
+ * the benchmark's CPU-baseline leg and reference arm load it.  It shares no header, helper,
  * table or constant with the CUDA path.
  *
  * What the method computes (sources are the five web pages reporting the
