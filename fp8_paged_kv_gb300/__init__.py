@@ -328,9 +328,11 @@ def fpk_paged_decode_attn_fp8_noalloc(q, kv_pool, k_scale, v_scale, page_table, 
 
 
 def fpk_decode_status(workspace, stream=None) -> int:
+    """Status word of an attention workspace; workspace=None reads the one of the
+    last allocation-free call on the current device."""
     v = ctypes.c_int32(0)
-    _check(load_library().fpk_decode_status(_ptr(workspace, _U8, "workspace"), ctypes.byref(v),
-                                            _stream(stream)), "fpk_decode_status")
+    _check(load_library().fpk_decode_status(_ptr(workspace, _U8, "workspace", allow_none=True),
+                                            ctypes.byref(v), _stream(stream)), "fpk_decode_status")
     return int(v.value)
 
 

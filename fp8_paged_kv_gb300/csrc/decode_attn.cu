@@ -1342,6 +1342,27 @@ int launch_split_kernel(const AttnArgs& a, int dev, int ctas, cudaStream_t s, bo
   return checked_launch_status();
 }
 
+// Shapes, required pointers and alignment of an attention call; no CUDA call
+// is made, so a rejected call has queued nothing.  need_workspace: the caller
+// supplies the workspace (the allocation-free entry point does not).
+template <bool kFp8>
+int check_attn_args(const void* q, const void* kv_pool, const float* k_scale, const float* v_scale,
+                    const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                    const float* out, const void* workspace, bool need_workspace, int32_t num_splits,
+                    int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                    int32_t num_pages) {
+  int st = check_attn_shapes(B, Hq, Hkv, D, page_size, num_pages, max_pages, num_splits);
+  if (st != FPK_OK) return st;
+  if (B == 0) return FPK_OK;
+  if (!q || !kv_pool || !page_table || !seq_lens || !out || (need_workspace && !workspace))
+    return FPK_EINVAL;
+  if (kFp8 && (!k_scale || !v_scale)) return FPK_EINVAL;
+  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FPK_EINVAL;
+  return FPK_OK;
+}
+
 template <bool kFp8>
 int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
                const float* v_scale, const int32_t* page_table, int32_t max_pages,
@@ -1349,14 +1370,9 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
                void* workspace, size_t workspace_bytes, int32_t num_splits, float sm_scale,
                int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
                int32_t num_pages, void* stream, AttnLaunch mode = AttnLaunch::kPlain) {
-  int st = check_attn_shapes(B, Hq, Hkv, D, page_size, num_pages, max_pages, num_splits);
-  if (st != FPK_OK) return st;
-  if (B == 0) return FPK_OK;
-  if (!q || !kv_pool || !page_table || !seq_lens || !out || !workspace) return FPK_EINVAL;
-  if (kFp8 && (!k_scale || !v_scale)) return FPK_EINVAL;
-  if (!aligned16(q) || !aligned16(kv_pool) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return FPK_EINVAL;
+  int st = check_attn_args<kFp8>(q, kv_pool, k_scale, v_scale, page_table, max_pages, seq_lens, out,
+                                 workspace, true, num_splits, B, Hq, Hkv, D, page_size, num_pages);
+  if (st != FPK_OK || B == 0) return st;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FPK_ECUDA;
   const int per_sm = prepare_kernel<kFp8>(dev);
@@ -1497,15 +1513,6 @@ extern "C" int fpk_decode_step_bf16(const void* k_new, const void* v_new, void* 
                                fpk::AttnLaunch::kAfterStepWrite);
 }
 
-extern "C" int fpk_decode_status(const void* workspace, int32_t* status, void* stream) {
-  if (!workspace || !status) return FPK_EINVAL;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return FPK_ECUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return FPK_ECUDA;
-  return FPK_OK;
-}
-
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the FP8 attention entry point.
 //
@@ -1527,19 +1534,59 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The array's device address, looked up once per device and context: a device
+// reset (or a primary context released and retained again) gives the device a
+// new context, in which the module and its array are loaded afresh.
+struct NoAllocSlot {
+  unsigned long long ctx_id;
+  void* addr;
+};
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+NoAllocSlot g_noalloc_slot[kMaxDevices];
 
-// Set-up, once per device: the scratch array's device address on `dev`
-// (which must be the current device).
+// Identity of the calling thread's current context (0 if it cannot be had):
+// the driver's context id, which no later context reuses.
+unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != 0 || ctx == nullptr ||
+      get_id(ctx, &id) != 0)
+    return 0;
+  return id;
+}
+
+// Set-up, once per device (and context): the scratch array's device address
+// on `dev`, which must be the current device.  Without a context id the
+// address is looked up on every call.
 int noalloc_scratch_address(int dev, void** addr) {
+  // before the runtime's first call on this device there may be no current
+  // context (id 0); the symbol lookup creates it, so the id kept is read after
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  NoAllocSlot& slot = g_noalloc_slot[dev];
+  const unsigned long long id = current_context_id();
+  if (slot.addr == nullptr || id == 0 || slot.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FPK_ECUDA;
-    g_noalloc_addr[dev] = p;
+    slot.addr = p;
+    slot.ctx_id = current_context_id();
   }
-  *addr = g_noalloc_addr[dev];
+  *addr = slot.addr;
   return FPK_OK;
 }
 
@@ -1555,9 +1602,11 @@ extern "C" int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k
                                                  int32_t Hq, int32_t Hkv, int32_t D,
                                                  int32_t page_size, int32_t num_pages,
                                                  void* stream) {
-  int st = fpk::check_attn_shapes(B, Hq, Hkv, D, page_size, num_pages, max_pages, num_splits);
-  if (st != FPK_OK) return st;
-  if (B == 0) return FPK_OK;
+  // every argument is checked before any CUDA call: a rejected call queues nothing
+  int st = fpk::check_attn_args<true>(q, kv_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
+                                      out, nullptr, false, num_splits, B, Hq, Hkv, D, page_size,
+                                      num_pages);
+  if (st != FPK_OK || B == 0) return st;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fpk::kMaxDevices) return FPK_ECUDA;
   void* scratch = nullptr;
@@ -1578,4 +1627,23 @@ extern "C" int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* k
   return fpk::attn_entry<true>(q, kv_pool, k_scale, v_scale, page_table, max_pages, seq_lens,
                                abort_mask, out, lse, scratch, fpk::kNoAllocScratchBytes, num_splits, sm_scale,
                                B, Hq, Hkv, D, page_size, num_pages, stream);
+}
+
+extern "C" int fpk_decode_status(const void* workspace, int32_t* status, void* stream) {
+  if (!status) return FPK_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* src = workspace;
+  if (src == nullptr) {
+    // the allocation-free entry point's scratch on the current device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fpk::kMaxDevices) return FPK_ECUDA;
+    void* addr = nullptr;
+    const int st = fpk::noalloc_scratch_address(dev, &addr);
+    if (st != FPK_OK) return st;
+    src = addr;
+  }
+  if (cudaMemcpyAsync(status, src, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FPK_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FPK_ECUDA;
+  return FPK_OK;
 }

@@ -23,13 +23,14 @@ __global__ void __launch_bounds__(256) bump_kernel(uint32_t* __restrict__ live_t
   if (p >= 0 && p < num_pages) atomicAdd(live_tags + p, 1u);
 }
 
-__global__ void __launch_bounds__(kValidateThreads) validate_kernel(
+// One request per cluster of `nparts` CTAs (one CTA for short tables).
+__global__ void __launch_bounds__(kValidateThreads, kCheckCtasPerSm) validate_kernel(
     const int32_t* __restrict__ page_table, const uint32_t* __restrict__ expected_tags,
     const int32_t* __restrict__ seq_lens, int max_pages, const uint32_t* __restrict__ live_tags,
-    int num_pages, int page_size, uint8_t* __restrict__ abort_mask, int32_t* __restrict__ abort_count) {
-  const int bad = check_request(page_table, expected_tags, seq_lens, max_pages, live_tags, num_pages,
-                                page_size, abort_mask, blockIdx.x);
-  if (threadIdx.x == 0 && bad && abort_count != nullptr) atomicAdd(abort_count, 1);
+    int num_pages, int page_size, uint8_t* __restrict__ abort_mask, int32_t* __restrict__ abort_count,
+    int nparts) {
+  check_request(page_table, expected_tags, seq_lens, max_pages, live_tags, num_pages, page_size,
+                abort_mask, abort_count, nparts);
 }
 
 }  // namespace
@@ -51,13 +52,16 @@ extern "C" int fpk_page_tags_validate(const int32_t* page_table, const uint32_t*
                                       int32_t page_size, uint8_t* abort_mask, int32_t* abort_count,
                                       void* stream) {
   if (B < 0 || max_pages < 0 || num_pages < 0 || page_size <= 0) return FPK_EINVAL;
+  // a rejected call queues nothing; with B == 0 the count is still zeroed
+  if (B > 0 && (!page_table || !expected_tags || !seq_lens || !live_tags || !abort_mask))
+    return FPK_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (abort_count != nullptr && cudaMemsetAsync(abort_count, 0, sizeof(int32_t), s) != cudaSuccess)
     return FPK_ECUDA;
   if (B == 0) return FPK_OK;
-  if (!page_table || !expected_tags || !seq_lens || !live_tags || !abort_mask) return FPK_EINVAL;
-  fpk::validate_kernel<<<B, fpk::kValidateThreads, 0, s>>>(page_table, expected_tags, seq_lens,
-                                                           max_pages, live_tags, num_pages,
-                                                           page_size, abort_mask, abort_count);
-  return fpk::checked_launch_status();
+  const int nparts = fpk::check_parts(max_pages, B);
+  if (static_cast<int64_t>(B) * nparts > 0x7fffffff) return FPK_EINVAL;
+  return fpk::launch_check_grid(fpk::validate_kernel, B * nparts, nparts, s, page_table, expected_tags,
+                                seq_lens, max_pages, live_tags, num_pages, page_size, abort_mask,
+                                abort_count, nparts);
 }

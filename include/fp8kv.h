@@ -385,11 +385,16 @@ int fpk_decode_step_bf16(const void* k_new, const void* v_new, void* kv_pool,
  * cudaMalloc, no cudaFree, no allocating library routine.
  * Set-up: the first call on a device looks up the array's device address on
  * that device (the device current at the call); make that first call before
- * any stream capture.
+ * any stream capture.  The address is kept per device and context: after a
+ * device reset the next call looks it up again (set-up again, so again
+ * outside any capture).
  * Sharing: every call on a device uses the same array and clears its status
  * word and counters first; calls that overlap on the GPU (other streams or
- * other host threads) race on it and must be serialised by the caller.  The
- * kernel's status word is not reported by this entry point.
+ * other host threads) race on it and must be serialised by the caller.
+ * Errors: arguments are checked before any CUDA call, so a rejected call
+ * queues nothing.  The kernel's status word (a bounded wait that gave up
+ * leaves some out/lse rows unwritten) stays in the scratch until the next
+ * call: read it with fpk_decode_status(NULL, ...) on the same device.
  */
 int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* kv_pool,
                                       const float* k_scale, const float* v_scale,
@@ -402,6 +407,8 @@ int fpk_paged_decode_attn_fp8_noalloc(const void* q, const uint8_t* kv_pool,
 /*
  * Copies the workspace status word to *status (HOST pointer) and synchronises
  * the stream.  0 means no bounded wait inside the attention kernels gave up.
+ * workspace == NULL reads the status word of the last
+ * fpk_paged_decode_attn_fp8_noalloc call on the current device instead.
  */
 int fpk_decode_status(const void* workspace, int32_t* status, void* stream);
 

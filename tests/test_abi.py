@@ -172,6 +172,28 @@ def test_attention_argument_errors_before_any_device_call():
     assert bf16(out=A + 4) == EINVAL and bf16(ws=None) == EINVAL
     assert bf16(B=0, q=None) == OK
 
+    # the allocation-free entry point checks the same arguments (it has no
+    # workspace) before it looks up its scratch or clears it
+    def noalloc(q=A, kv=A, ks=A, vs=A, pt=A, lens=A, out=A, B=2, Hq=16, Hkv=2, D=128, ps=16,
+                splits=0):
+        return lib.fpk_paged_decode_attn_fp8_noalloc(q, kv, ks, vs, pt, 4, lens, None, out, None,
+                                                     splits, 0.1, B, Hq, Hkv, D, ps, 8, None)
+
+    assert noalloc(B=0, q=None, kv=None, out=None) == OK
+    assert noalloc(Hq=15) == EINVAL and noalloc(B=-1) == EINVAL and noalloc(splits=-1) == EINVAL
+    assert noalloc(D=64) == EUNSUP and noalloc(ps=24) == EUNSUP
+    for name in ("q", "kv", "ks", "vs", "pt", "lens", "out"):
+        assert noalloc(**{name: None}) == EINVAL, name
+    assert noalloc(q=A + 2) == EINVAL and noalloc(kv=A + 8) == EINVAL and noalloc(out=A + 4) == EINVAL
+
+    # the tag check rejects missing tables before it clears the abort count
+    def validate(pt=A, ex=A, lens=A, live=A, mask=A, count=A, B=2):
+        return lib.fpk_page_tags_validate(pt, ex, lens, 4, live, 8, B, 16, mask, count, None)
+
+    for name in ("pt", "ex", "lens", "live", "mask"):
+        assert validate(**{name: None}) == EINVAL, name
+    assert validate(B=-1) == EINVAL
+
 
 def test_write_and_gemv_argument_errors_before_any_device_call():
     """The same for the cache writes and the weight GEMV: every call below
