@@ -19,19 +19,22 @@ namespace {
 
 constexpr int kWriteCtas = 64;  // CTAs that share the token writes (grid-stride)
 
+// CTAs [0, B * nparts) check one request per cluster of nparts CTAs; the
+// rest (a multiple of nparts, in clusters that hold no barrier) write tokens.
 template <bool kFp8>
-__global__ void __launch_bounds__(kValidateThreads) append_check_kernel(WriteArgs w,
+__global__ void __launch_bounds__(kValidateThreads, kCheckCtasPerSm) append_check_kernel(WriteArgs w,
                                                                         const uint32_t* live_tags,
                                                                         const uint32_t* expected_tags,
-                                                                        uint8_t* abort_mask) {
+                                                                        uint8_t* abort_mask,
+                                                                        int nparts) {
   // a programmatically dependent attention launch may start its set-up now;
   // it reads nothing this kernel writes before this grid has completed
   griddep_launch_dependents();
   // no tags: the no-op tracker -- no check CTAs, unguarded writes
-  const int nchk = (live_tags != nullptr && expected_tags != nullptr) ? w.B : 0;
+  const int nchk = (live_tags != nullptr && expected_tags != nullptr) ? w.B * nparts : 0;
   if (static_cast<int>(blockIdx.x) < nchk) {
     check_request(w.page_table, expected_tags, w.seq_lens, w.max_pages, live_tags, w.num_pages,
-                  w.page_size, abort_mask, blockIdx.x);
+                  w.page_size, abort_mask, nullptr, nparts);
     return;
   }
   const int64_t units = w.rows * w.Hkv * (w.D >> 3);
@@ -82,11 +85,17 @@ int append_check_entry(bool fp8, const void* k_new, const void* v_new, void* kv_
   w.max_pages = max_pages;
   const int64_t units = static_cast<int64_t>(B) * Hkv * (D >> 3);
   const int64_t want = (units + kValidateThreads - 1) / kValidateThreads;
-  const int grid = (check ? B : 0) + static_cast<int>(want < kWriteCtas ? want : kWriteCtas);
+  const int nparts = check ? check_parts(max_pages, B) : 1;
+  // write CTAs rounded up to whole clusters
+  const int64_t nwrite = ((want < kWriteCtas ? want : kWriteCtas) + nparts - 1) / nparts * nparts;
+  const int64_t grid = (check ? static_cast<int64_t>(B) * nparts : 0) + nwrite;
+  if (grid > 0x7fffffff) return FPK_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (fp8) append_check_kernel<true><<<grid, kValidateThreads, 0, s>>>(w, w.live_tags, w.expected_tags, w.abort_mask);
-  else append_check_kernel<false><<<grid, kValidateThreads, 0, s>>>(w, w.live_tags, w.expected_tags, w.abort_mask);
-  return checked_launch_status();
+  if (fp8)
+    return launch_check_grid(append_check_kernel<true>, static_cast<int>(grid), nparts, s, w, w.live_tags,
+                             w.expected_tags, w.abort_mask, nparts);
+  return launch_check_grid(append_check_kernel<false>, static_cast<int>(grid), nparts, s, w, w.live_tags,
+                           w.expected_tags, w.abort_mask, nparts);
 }
 
 }  // namespace fpk

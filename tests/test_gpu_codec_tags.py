@@ -130,7 +130,8 @@ def test_bump_bit_exact():
     assert np.array_equal(d_live.cpu().numpy().view(np.uint32), live)
 
 
-@pytest.mark.parametrize("B,max_pages,ps", [(3, 4, 16), (64, 1040, 16), (256, 600, 16), (7, 33, 64)])
+@pytest.mark.parametrize("B,max_pages,ps", [(3, 4, 16), (64, 1040, 16), (256, 600, 16), (7, 33, 64),
+                                            (4, 2048, 64), (5, 300, 16), (9, 700, 16), (2, 20000, 16)])
 def test_validate_abort_sets_bit_exact(B, max_pages, ps):
     g = rng_for(53, "validate", B)
     num_pages = B * max_pages + 17
@@ -175,6 +176,36 @@ def test_validate_abort_sets_bit_exact(B, max_pages, ps):
     assert int(d_cnt.item()) == n
 
 
+@pytest.mark.parametrize("max_pages", [2048, 5000, 9000, 20000])
+def test_validate_long_tables_every_part(max_pages):
+    # tables above 4096 entries are shared by a cluster of 2, 4 or 8 CTAs
+    # (thread t of part k takes entries k*256 + t + j*parts*256); request r
+    # carries one corruption in entries r*256 .. r*256+255, which fall to part
+    # r mod parts (request 8: none; request 9: its last entry), so every
+    # part's finding must reach the request's abort flag, and only its own
+    ps = 16
+    B = 10
+    g = rng_for(54, "parts", max_pages)
+    num_pages = B * max_pages
+    pt = g.permutation(num_pages).astype(np.int32).reshape(B, max_pages)
+    live = g.integers(0, 2**32, size=num_pages, dtype=np.uint64).astype(np.uint32)
+    ex = live[pt]
+    lens = np.full(B, max_pages * ps, np.int32)
+    for r in range(8):
+        i = r * 256 + int(g.integers(0, 256))
+        if i < max_pages:
+            ex[r, i] ^= np.uint32(1 << (r % 32))
+    ex[9, max_pages - 1] -= np.uint32(1)
+    want, n = oracle.page_tags_validate(pt, ex, lens, live, num_pages, ps)
+    d_mask = torch.full((B,), 7, dtype=torch.uint8, device=DEV)
+    d_cnt = torch.full((1,), -5, dtype=torch.int32, device=DEV)
+    fpk_page_tags_validate(to_device(pt, DEV), to_device(ex, DEV), to_device(lens, DEV),
+                           to_device(live, DEV), d_mask, d_cnt, num_pages=num_pages, page_size=ps)
+    got = d_mask.cpu().numpy()
+    assert np.array_equal(got, want) and int(d_cnt.item()) == n
+    assert got[8] == 0 and got[9] == 1
+
+
 def test_tiny_workload_abort_set():
     wl = tiny()
     pool = DecodePool(wl, fp8=True, device=DEV)
@@ -191,11 +222,15 @@ def test_tiny_workload_abort_set():
 
 @pytest.mark.parametrize("fp8", [True, False])
 @pytest.mark.parametrize("what", ["none", "stale_last", "stale_inner", "page_oob", "beyond_table"])
-def test_append_check_one_launch_equals_write_then_check(fp8, what):
+@pytest.mark.parametrize("table", ["short", "long"])
+def test_append_check_one_launch_equals_write_then_check(fp8, what, table):
     """fpk_decode_append_check_*: bytes and abort mask equal to the oracle's append followed
-    by its batched check, for clean tables and every kind of bad entry."""
+    by its batched check, for clean tables and every kind of bad entry; long tables are
+    checked by a cluster of CTAs per request."""
     ps = 16
-    wl = custom(54, B=6, Hq=8, Hkv=2, ps=ps, prompt_lens=[20, 40, 15, 31, 0, 300], steps=1)
+    # long: 6251 table entries, checked by a cluster of two CTAs per request
+    lens0 = [20, 40, 15, 31, 0, 300] if table == "short" else [20, 8000, 15, 31, 0, 100000]
+    wl = custom(54, B=6, Hq=8, Hkv=2, ps=ps, prompt_lens=lens0, steps=1)
     pt, ex = wl.page_table.copy(), wl.expected_tags.copy()
     lens = wl.seq_lens_after(0).copy()
     r = 1
