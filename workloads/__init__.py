@@ -182,16 +182,25 @@ def _build(name, seed, B, Hq, Hkv, ps, prompt_lens, steps, num_pages, *, sigma=1
     N = int(cu[-1])
     kp = np.empty((N, Hkv, D), np.uint16)
     vp = np.empty((N, Hkv, D), np.uint16)
+
+    def fill(job):
+        # one chunk of one prompt from its own stream: K rows, then V rows
+        r, c = job
+        n0 = c * PROMPT_CHUNK
+        n1 = min(int(prompt_lens[r]), n0 + PROMPT_CHUNK)
+        g = rng_for(seed, "prompt", r, c)
+        amax = []
+        for dst in (kp, vp):
+            x = wl._draw(g, (n1 - n0, Hkv, D))
+            dst[cu[r] + n0:cu[r] + n1] = bf16_bits(x)
+            amax.append(_amax_bf16(x))
+        return amax
+
+    jobs = [(r, c) for r in range(B) for c in range(-(-int(prompt_lens[r]) // PROMPT_CHUNK))]
     kmax = vmax = 0.0
-    for r in range(B):
-        g = rng_for(seed, "prompt", r)
-        k = bf16_bits(wl._draw(g, (int(prompt_lens[r]), Hkv, D)))
-        v = bf16_bits(wl._draw(g, (int(prompt_lens[r]), Hkv, D)))
-        kp[cu[r]:cu[r + 1]] = k
-        vp[cu[r]:cu[r + 1]] = v
-        if k.size:
-            kmax = max(kmax, float(np.abs(bf16_to_f32(k)).max()))
-            vmax = max(vmax, float(np.abs(bf16_to_f32(v)).max()))
+    with _draw_pool() as ex:
+        for km, vm in ex.map(fill, jobs):
+            kmax, vmax = max(kmax, km), max(vmax, vm)
     for s in range(steps):
         k, v = wl.step_tokens(s)
         kmax = max(kmax, float(np.abs(bf16_to_f32(k)).max()))
@@ -199,6 +208,27 @@ def _build(name, seed, B, Hq, Hkv, ps, prompt_lens, steps, num_pages, *, sigma=1
     wl.k_prompt, wl.v_prompt = kp, vp
     wl.k_scale, wl.v_scale = _scale_of(kmax), _scale_of(vmax)
     return wl
+
+
+# tokens of a prompt drawn from one stream; chunks are drawn in parallel
+PROMPT_CHUNK = 4096
+
+
+def _amax_bf16(x: np.ndarray) -> float:
+    """max |bf16(x)| over a float32 array: rounding to nearest is monotonic in
+    |x|, so it is the rounding of max |x|."""
+    if x.size == 0:
+        return 0.0
+    m = np.float32(max(float(x.max()), -float(x.min())))
+    return float(bf16_to_f32(bf16_bits(np.array([m], np.float32)))[0])
+
+
+def _draw_pool():
+    """Threads for drawing prompt chunks (numpy's generators and ufuncs release
+    the interpreter lock on large arrays)."""
+    import concurrent.futures as cf
+    import os
+    return cf.ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
 
 
 def tiny(seed: int = 1) -> Workload:
