@@ -505,24 +505,32 @@ def time_prefill(pool, reps: int = 5):
             "amax_scale_gbs": amax_bytes / (res[1] * 1e-3) / 1e9}
 
 
-def time_e2e(pool, steps: int, warmup: int):
-    """Same step through the public API with host buffers: pinned H2D of the step's
-    inputs (q, new K/V rows, context lengths: one buffer, one copy), the step, D2H of
-    out/lse/abort mask (one buffer, one copy)."""
-    h_in = pool.io_in.cpu().pin_memory()
-    h_out = torch.empty_like(pool.io_out, device="cpu").pin_memory()
-    h2d = h_in.numel() * h_in.element_size()
-    d2h = h_out.numel() * h_out.element_size()
-
-    def h2d_copies():
-        pool.io_in.copy_(h_in, non_blocking=True)
-
-    def d2h_copies():
-        h_out.copy_(pool.io_out, non_blocking=True)
-
-    g = capture_step(pool, True, io=(h2d_copies, d2h_copies))
-    ms = time_graph(g, steps, warmup)
-    return ms, h2d, d2h
+def time_e2e(pool, steps: int, warmup: int, depth: int = 16):
+    """The step through the public API with host buffers (DecodePool +
+    HostPipeline): every step copies its own inputs (q, new K/V rows, context
+    lengths: one buffer) in from pinned host memory and its results (out, lse,
+    abort mask: one buffer) back out, with step i+1's copy-in and step i-1's
+    copy-out under step i's kernels.  `depth` steps (each with its own host
+    buffers) are captured as one CUDA graph and replayed."""
+    from fp8_paged_kv_gb300.pool import HostPipeline
+    src = pool.io_in.cpu()
+    h_in = [src.clone().pin_memory() for _ in range(depth)]
+    h_out = [torch.empty_like(pool.io_out, device="cpu").pin_memory() for _ in range(depth)]
+    pipe = HostPipeline(pool, h_in, h_out, validate=True)
+    h2d, d2h = pipe.bytes_per_step()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        pipe.run(depth)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pipe.run(depth)
+    torch.cuda.synchronize()
+    reps = max(1, -(-steps // depth))
+    ms = time_graph(g, reps, max(1, -(-warmup // depth))) / depth
+    return ms, h2d, d2h, reps * depth
 
 
 class L2Flush:
@@ -688,6 +696,217 @@ def local_rank() -> int:
     return int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def validation_overhead(g_val, g_noval, pairs: int, replays: int):
+    """Share of the step the tag check adds: the single-step graph with and
+    without the check (same inputs, same kernels, the check's CTAs absent),
+    timed as `pairs` interleaved pairs of `replays` replays each (the order
+    inside a pair alternates).  Reports the median and quartiles of the
+    per-pair relative differences."""
+    d, tv, tn = [], [], []
+    for i in range(pairs):
+        if i % 2 == 0:
+            a = time_graph(g_val, replays, 3)
+            b = time_graph(g_noval, replays, 3)
+        else:
+            b = time_graph(g_noval, replays, 3)
+            a = time_graph(g_val, replays, 3)
+        tv.append(a)
+        tn.append(b)
+        d.append(100.0 * (a - b) / b)
+    q1, med, q3 = (float(x) for x in np.percentile(d, [25, 50, 75]))
+    return {"median_pct": med, "q1_pct": q1, "q3_pct": q3, "pairs": pairs, "replays_per_side": replays,
+            "step_us_with": 1e3 * statistics.median(tv), "step_us_without": 1e3 * statistics.median(tn)}
+
+
+def time_attention_sequence(pool, staged, nsteps: int):
+    """Attention launches of decode steps 0..nsteps-1, each timed with events on
+    its stream after that step's inputs were staged and its write + check ran;
+    returns (mean attention ms, mean write + check ms)."""
+    K, V, Q, lens = staged
+    s = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nsteps)]
+    for i in range(nsteps):
+        pool.seq_lens.copy_(lens[i])
+        pool.k_new.copy_(K[i])
+        pool.v_new.copy_(V[i])
+        pool.q.copy_(Q[i])
+        ev[i][0].record(s)
+        pool.append_check(stream=s)
+        ev[i][1].record(s)
+        ev[i][2].record(s)
+        pool.attend(use_mask=True, stream=s)
+        ev[i][3].record(s)
+    torch.cuda.synchronize()
+    return (statistics.mean(e[2].elapsed_time(e[3]) for e in ev),
+            statistics.mean(e[0].elapsed_time(e[1]) for e in ev))
+
+
+def roofline(abytes: float, attn_ms: float, name: str, peak: float, peak_kind: str):
+    achieved = abytes / (attn_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": read_profile_traffic(name, "fp8"), "algorithmic_bytes": int(abytes),
+            "kernel": "paged_decode attention (split-KV, FP8)",
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+
+def measure_fp8(wl, args, world, local, headline: bool):
+    """The FP8 decode step of one workload: step time (CUDA graph; a growing
+    workload replays all its decode steps as one graph), the attention
+    launch's own time and roofline, the tag check's share of the step, and for
+    the headline workload also the end-to-end figure and the prompt write."""
+    import fp8_paged_kv_gb300 as fpk
+    from fp8_paged_kv_gb300.pool import DecodePool
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pool = DecodePool(wl, fp8=True, device=dev)
+    pool.prefill()
+    pool.set_step(0)
+    pool.step()
+    torch.cuda.synchronize()
+    live = int(wl.B - int(pool.abort_count.item()))
+    # the decode step as one CUDA graph (cache write and tag check in one launch,
+    # attention after it); the mismatch count is taken on the host from the abort
+    # mask the step returns
+    pool.count_aborts = False
+    g_step = capture_step(pool, True)
+    g_noval = capture_step(pool, False)
+    seq_steps = wl.steps if wl.steps > 1 else 0
+    g_seq = staged = None
+    if seq_steps:
+        g_seq, staged = capture_steps_sequence(pool, seq_steps)
+    barrier(world)
+    torch.cuda.synchronize()
+    peak, peak_kind = measured_peaks()
+    res = {}
+    with ClockSampler(local) as clk:
+        if g_seq is None:
+            timed_steps = args.steps
+            ms_step = time_graph(g_step, args.steps, args.warmup)
+        else:
+            reps = max(1, -(-args.steps // seq_steps))
+            timed_steps = reps * seq_steps
+            ms_step = time_graph(g_seq, reps, 1) / seq_steps
+        barrier(world)
+        ms_step = max_over_ranks(ms_step, world)
+        # the attention launch alone, with events between the launches on their
+        # stream: at decode step 0, or over every step of a growing workload
+        if staged is None:
+            pool.set_step(0)
+            _, attn_ms, app_ms = time_steps(pool, max(args.steps // 4, 20), 3)
+            abytes = attention_bytes(wl, 0, True)
+        else:
+            attn_ms, app_ms = time_attention_sequence(pool, staged, seq_steps)
+            abytes = statistics.mean(attention_bytes(wl, s_, True) for s_ in range(seq_steps))
+            pool.set_step(0)
+        val = validation_overhead(g_step, g_noval, args.val_pairs, args.val_replays)
+        status = fpk.fpk_decode_status(pool.workspace)
+        if headline:
+            e2e_ms, h2d, d2h, e2e_steps = time_e2e(pool, max(args.steps, 64), 16)
+            e2e_ms = max_over_ranks(e2e_ms, world)
+    res.update({
+        "workload": workload_config(wl)["workload"], "ms_per_step": ms_step, "timed_steps": timed_steps,
+        "tokens_per_s": live * world / (ms_step * 1e-3),
+        "step_launch": ("one CUDA graph per step" if g_seq is None
+                        else f"all {seq_steps} decode steps as one CUDA graph (inputs staged on the device)"),
+        "attn_us": attn_ms * 1e3, "append_and_check_us": app_ms * 1e3,
+        "attn_tokens_per_s": live * world / (attn_ms * 1e-3),
+        "roofline": roofline(abytes, attn_ms, wl.name, peak, peak_kind),
+        "validation_overhead_pct": val["median_pct"], "validation_overhead": val,
+        "status_word": status, "clocks": clk.summary(), "live_requests": live})
+    if wl.num_splits:
+        res["num_splits"] = wl.num_splits
+    if headline:
+        res["e2e"] = {"value": live * world / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "timed_steps": e2e_steps,
+                      "api": "DecodePool + HostPipeline: pinned host buffers per step, copies on a second "
+                             "stream overlapping the neighbouring steps' kernels, 16 steps per CUDA graph"}
+        res["prefill"] = time_prefill(pool)
+    if wl.name == "long128k":
+        # the same launch with the automatic split count (one wave of CTAs)
+        pool.set_step(0)
+        pool.num_splits = 0
+        pool.workspace = torch.zeros(max(256, fpk.fpk_decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, 0)),
+                                     dtype=torch.uint8, device=dev)
+        _, a_auto, _ = time_steps(pool, 20, 3)
+        res["attn_us_auto_splits"] = a_auto * 1e3
+        res["roofline_auto_splits_frac"] = attention_bytes(wl, 0, True) / (a_auto * 1e-3) / 1e9 / peak
+    del pool
+    torch.cuda.empty_cache()
+    return res
+
+
+def capacity_summary(args, local):
+    """Admission at a fixed one-layer KV budget, compactly: each cache's cap in
+    8192-token requests of the headline shape and its decode-attention tokens/s
+    at the cap and at 32 requests (where both fit).  Cache values are random
+    codes (only timing is taken); L2 is flushed before every timed launch."""
+    import fp8_paged_kv_gb300 as fpk
+    from fp8_paged_kv_gb300.pool import admission_cap
+    dev = torch.device("cuda", torch.cuda.current_device())
+    Hq, Hkv, D, ps, L = 64, 8, 128, 16, 8192
+    budget = int(args.kv_budget_gib * 2**30)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    flush = L2Flush(dev)
+    s = torch.cuda.current_stream(dev)
+    res = {"kv_budget_gib": args.kv_budget_gib, "context": L,
+           "shape": f"Hq={Hq}, Hkv={Hkv}, D={D}, page_size={ps}, one layer", "l2": L2Flush.NOTE}
+    with ClockSampler(local) as clk:
+        for fp8 in (False, True):
+            num_pages, ppr, cap = admission_cap(budget, L, Hkv=Hkv, D=D, page_size=ps, fp8=fp8)
+            n = num_pages * 2 * Hkv * ps * D
+            if fp8:
+                pool = torch.randint(0, 0x7F, (n,), dtype=torch.uint8, device=dev, generator=g)
+                pool |= torch.randint(0, 2, (n,), dtype=torch.uint8, device=dev, generator=g) << 7
+            else:
+                pool = torch.randn(n, device=dev, generator=g, dtype=torch.bfloat16)
+            perm = torch.randperm(num_pages, device=dev, generator=g).to(torch.int32)
+            pts = {}
+            for c in sorted({32, cap}):
+                if c > cap:
+                    continue
+                pt = perm[:c * ppr].view(c, ppr).contiguous()
+                lens = torch.full((c,), L, dtype=torch.int32, device=dev)
+                q = torch.randn(c, Hq, D, device=dev, generator=g).to(torch.bfloat16)
+                out = torch.empty(c, Hq, D, device=dev)
+                lse = torch.empty(c, Hq, device=dev)
+                ws = torch.zeros(fpk.fpk_decode_workspace_bytes(c, Hq, Hkv, D, 0), dtype=torch.uint8,
+                                 device=dev)
+                ks = torch.tensor([0.01], device=dev)
+                kw = dict(Hkv=Hkv, page_size=ps, num_pages=num_pages, sm_scale=D ** -0.5)
+                t = []
+                for i in range(3 + args.capacity_reps):
+                    flush()
+                    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(s)
+                    if fp8:
+                        fpk.fpk_paged_decode_attn_fp8(q, pool, ks, ks, pt, lens, None, out, lse, ws, **kw)
+                    else:
+                        fpk.fpk_paged_decode_attn_bf16(q, pool, pt, lens, None, out, lse, ws, **kw)
+                    e.record(s)
+                    torch.cuda.synchronize(dev)
+                    if i >= 3:
+                        t.append(a.elapsed_time(e))
+                ms = statistics.median(t)
+                kv = c * L * 2 * Hkv * D * (1 if fp8 else 2)
+                nbytes = kv + c * ppr * 4 + c * Hq * D * 2 + c * Hq * (D + 1) * 4
+                pts["at_cap" if c == cap else "at_32"] = {"requests": c, "attn_us": ms * 1e3,
+                                                          "tokens_per_s": c / (ms * 1e-3),
+                                                          "gbs": nbytes / (ms * 1e-3) / 1e9}
+                if c == 32 and cap == 32:
+                    pts["at_32"] = pts["at_cap"]
+                del ws, q, out, lse
+            res["fp8" if fp8 else "bf16"] = {"pool_pages": num_pages, "pages_per_request": ppr,
+                                             "cap_requests": cap, **pts}
+            del pool, perm
+            torch.cuda.empty_cache()
+    res["fp8_over_bf16_cap"] = res["fp8"]["cap_requests"] / max(1, res["bf16"]["cap_requests"])
+    res["fp8_at_cap_over_bf16_at_cap_tokens_per_s"] = (res["fp8"]["at_cap"]["tokens_per_s"] /
+                                                       res["bf16"]["at_cap"]["tokens_per_s"])
+    res["clocks"] = clk.summary()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -697,6 +916,12 @@ def main():
     ap.add_argument("--workload", default="b32_8k")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads' objects and the capacity object")
+    ap.add_argument("--extra", default="b64_var,long128k",
+                    help="workloads measured beside the headline one (comma separated)")
+    ap.add_argument("--val-pairs", type=int, default=10)
+    ap.add_argument("--val-replays", type=int, default=100)
     ap.add_argument("--capacity", action="store_true",
                     help="admission curve at a fixed KV budget instead of the step benchmark")
     ap.add_argument("--kv-budget-gib", type=float, default=4.0)
@@ -728,97 +953,37 @@ def main():
         fbuild.build()
     barrier(world)
     fpk.load_library()
-    wl = WORKLOADS[args.workload](seed=100 + rank) if world > 1 else WORKLOADS[args.workload]()
-    if args.workload == "b64_var" and rank == 0:
-        print(f"# b64_var: {wl.steps} decode steps per graph replay", file=sys.stderr)
 
+    def make(name):
+        return WORKLOADS[name](seed=100 + rank) if world > 1 else WORKLOADS[name]()
+
+    wl = make(args.workload)
     # ---------------- FP8 cache: the measured path
-    pool = DecodePool(wl, fp8=True, device=torch.device("cuda", torch.cuda.current_device()))
-    pool.prefill()
-    pool.set_step(0)
-    pool.step()
-    torch.cuda.synchronize()
-    live = int(wl.B - int(pool.abort_count.item()))
-
-    # the decode step as one CUDA graph (cache write and tag check in one launch,
-    # attention after it); the mismatch count is taken on the host from the abort
-    # mask the step returns
-    pool.count_aborts = False
-    g_step = capture_step(pool, True)
-    g_noval = capture_step(pool, False)
-    seq_steps = wl.steps if wl.steps > 1 else 0
-    g_seq = None
-    if seq_steps:
-        # a growing workload: all its decode steps in one graph, replayed whole
-        g_seq, staged = capture_steps_sequence(pool, seq_steps)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        if g_seq is None:
-            timed_steps = args.steps
-            ms_step = time_graph(g_step, args.steps, args.warmup)
-        else:
-            reps = max(1, args.steps // seq_steps)
-            timed_steps = reps * seq_steps
-            ms_step = time_graph(g_seq, reps, max(1, args.warmup // seq_steps)) / seq_steps
-    barrier(world)
-    ms_step = max_over_ranks(ms_step, world)
-    value = live * world / (ms_step * 1e-3)
-
-    # per-kernel device times: the same step launched kernel by kernel, with events
-    # between the launches on their streams (the attention time is the roofline's),
-    # at decode step 0's inputs
-    pool.set_step(0)
-    _, attn_ms, app_ms = time_steps(pool, max(args.steps // 4, 20), 3)
-    # validation overhead: the single-step graph with and without the tag check,
-    # on the same inputs (decode step 0), interleaved to share clock conditions
-    nv = max(args.steps // 4, 20)
-    with_val, without_val = [], []
-    for _ in range(3):
-        with_val.append(time_graph(g_step, nv, 3))
-        without_val.append(time_graph(g_noval, nv, 3))
-    step_val = statistics.median(with_val)
-    noval_step = statistics.median(without_val)
-    status = fpk.fpk_decode_status(pool.workspace)
-
-    e2e_ms, h2d, d2h = time_e2e(pool, max(args.steps // 4, 20), 3)
-    e2e_ms = max_over_ranks(e2e_ms, world)
-    prefill = time_prefill(pool)
-
-    abytes = attention_bytes(wl, 0, True)
-    peak, peak_kind = measured_peaks()
-    achieved = abytes / (attn_ms * 1e-3) / 1e9
-    # attention-only throughput and GB/s
+    m = measure_fp8(wl, args, world, local, headline=True)
+    ms_step = m["ms_per_step"]
+    live = m["live_requests"]
     out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": m["tokens_per_s"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache; f16 MMA, fp32 softmax",
         "data": "synthetic", "config": workload_config(wl),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": read_profile_traffic(wl.name, "fp8"),
-                     "kernel": "paged_decode attention (split-KV, FP8)",
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
-        "fp8": {"attn_us": attn_ms * 1e3, "append_and_check_us": app_ms * 1e3,
-                "attn_tokens_per_s": live * world / (attn_ms * 1e-3),
-                "attn_gbs": achieved, "step_us_with_validation": step_val * 1e3, "step_us_without_validation": noval_step * 1e3,
-                "step_launch": "CUDA graph per step",
-                "validation_overhead_pct": 100.0 * (step_val - noval_step) / noval_step,
-                "algorithmic_bytes_per_attention": abytes, "status_word": status},
-        "gpu_launches": None, "clocks": clk.summary(),
-        "e2e": {"value": live * world / (e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "prefill": prefill,
+        "roofline": m["roofline"],
+        "fp8": {"attn_us": m["attn_us"], "append_and_check_us": m["append_and_check_us"],
+                "attn_tokens_per_s": m["attn_tokens_per_s"], "attn_gbs": m["roofline"]["achieved"],
+                "step_launch": m["step_launch"],
+                "validation_overhead_pct": m["validation_overhead_pct"],
+                "validation_overhead": m["validation_overhead"],
+                "algorithmic_bytes_per_attention": m["roofline"]["algorithmic_bytes"],
+                "status_word": m["status_word"]},
+        # per timed step: the cache write + tag check launch and the attention
+        # launch (the split combine runs inside the attention kernel)
+        "gpu_launches": 2 * m["timed_steps"], "clocks": m["clocks"],
+        "e2e": m["e2e"], "prefill": m["prefill"],
     }
-    # per timed step: the cache write + tag check launch and the attention launch
-    # (the split combine runs inside the attention kernel)
-    launches_per_step = 2
-    out["gpu_launches"] = launches_per_step * timed_steps
-    del pool
-    torch.cuda.empty_cache()
 
     # ---------------- BF16 cache on identical values
     if not args.no_bf16:
+        peak = m["roofline"]["peak"]
         p16 = DecodePool(wl, fp8=False, device=torch.device("cuda", torch.cuda.current_device()))
         p16.prefill()
         p16.set_step(0)
@@ -833,8 +998,16 @@ def main():
                        "attn_frac": b16 / (a16 * 1e-3) / 1e9 / peak,
                        "fp8_over_bf16_step": (t16 / n16) / ms_step,
                        "traffic": read_profile_traffic(wl.name, "bf16")}
-        del p16
+        del p16, g16
         torch.cuda.empty_cache()
+
+    # ---------------- the other workloads, each as its own object
+    if not args.no_extra:
+        for name in [n for n in args.extra.split(",") if n and n != args.workload]:
+            w2 = make(name)
+            out[name] = measure_fp8(w2, args, world, local, headline=False)
+            del w2
+        out["capacity"] = capacity_summary(args, local)
 
     if rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(wl)

@@ -66,16 +66,10 @@ class DecodePool:
         self.expected_tags = to_device(wl.expected_tags, dev)
         self.k_scale = torch.tensor([float(wl.k_scale)], dtype=torch.float32, device=dev)
         self.v_scale = torch.tensor([float(wl.v_scale)], dtype=torch.float32, device=dev)
-        # a step's inputs and results, each in one buffer (io_in, io_out)
-        self.io_in, v_in = _arena(dev, [("q", (wl.B, wl.Hq, wl.D), torch.bfloat16),
-                                        ("k_new", (wl.B, wl.Hkv, wl.D), torch.bfloat16),
-                                        ("v_new", (wl.B, wl.Hkv, wl.D), torch.bfloat16),
-                                        ("seq_lens", (wl.B,), torch.int32)])
-        self.io_out, v_out = _arena(dev, [("out", (wl.B, wl.Hq, wl.D), torch.float32),
-                                          ("lse", (wl.B, wl.Hq), torch.float32),
-                                          ("abort_mask", (wl.B,), torch.uint8)])
-        self.q, self.k_new, self.v_new, self.seq_lens = (v_in[k] for k in ("q", "k_new", "v_new", "seq_lens"))
-        self.out, self.lse, self.abort_mask = (v_out[k] for k in ("out", "lse", "abort_mask"))
+        # a step's inputs and results, each in one buffer (io_in, io_out); a
+        # second pair is made on demand for pipelined host steps (io_slot)
+        self._io = [self._new_io()]
+        self.io_slot(0)
         self.seq_lens.copy_(to_device(wl.prompt_lens.astype(np.int32), dev))
         self.q.copy_(to_device(wl.q, dev))
         self.abort_count = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -83,6 +77,25 @@ class DecodePool:
         ws = fpk_decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, self.num_splits)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
         self.count_aborts = True
+
+    def _new_io(self):
+        wl, dev = self.wl, self.device
+        io_in, v_in = _arena(dev, [("q", (wl.B, wl.Hq, wl.D), torch.bfloat16),
+                                   ("k_new", (wl.B, wl.Hkv, wl.D), torch.bfloat16),
+                                   ("v_new", (wl.B, wl.Hkv, wl.D), torch.bfloat16),
+                                   ("seq_lens", (wl.B,), torch.int32)])
+        io_out, v_out = _arena(dev, [("out", (wl.B, wl.Hq, wl.D), torch.float32),
+                                     ("lse", (wl.B, wl.Hq), torch.float32),
+                                     ("abort_mask", (wl.B,), torch.uint8)])
+        return io_in, v_in, io_out, v_out
+
+    def io_slot(self, i: int):
+        """Point the step's inputs and results at I/O buffer pair i (0 or 1)."""
+        while len(self._io) <= i:
+            self._io.append(self._new_io())
+        self.io_in, v_in, self.io_out, v_out = self._io[i]
+        self.q, self.k_new, self.v_new, self.seq_lens = (v_in[k] for k in ("q", "k_new", "v_new", "seq_lens"))
+        self.out, self.lse, self.abort_mask = (v_out[k] for k in ("out", "lse", "abort_mask"))
 
     @property
     def kw(self):
@@ -213,3 +226,97 @@ class DecodePool:
         if self.fp8:
             return self.kv_pool.cpu().numpy()
         return self.kv_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class HostPipeline:
+    """Decode steps fed from pinned host memory and drained back to it, with
+    the copies of neighbouring steps under each step's kernels.
+
+    Step i reads its inputs (q, new K/V rows, context lengths: one buffer)
+    from host_in[i % len(host_in)] and leaves its results (out, lse, abort
+    mask: one buffer) in host_out[i % len(host_out)].  The pool's two I/O
+    buffer pairs alternate between steps.  On a copy stream, step i+1's
+    inputs go in and step i-1's results come out while step i runs on the
+    compute stream; every step still copies its own inputs in and its own
+    results out.  Ordering, per buffer pair b = i % 2:
+      - copy-in of step i waits until step i-2 (the last user of pair b) ends;
+      - step i waits for its copy-in and for the copy-out of step i-2;
+      - copy-out of step i waits until step i ends.
+    run() only enqueues work (it can be captured in a CUDA graph); the host
+    buffers must be pinned and stay alive until the copies complete.
+    """
+
+    def __init__(self, pool: "DecodePool", host_in, host_out, validate: bool = True):
+        self.pool = pool
+        self.host_in = list(host_in)
+        self.host_out = list(host_out)
+        self.validate = validate
+        for h in self.host_in + self.host_out:
+            if h.is_cuda or not h.is_pinned():
+                raise ValueError("host buffers must be pinned host tensors")
+        pool.io_slot(1)
+        pool.io_slot(0)
+        if any(h.numel() * h.element_size() != pool.io_in.numel() for h in self.host_in) or \
+           any(h.numel() * h.element_size() != pool.io_out.numel() for h in self.host_out):
+            raise ValueError("host buffers must match the pool's I/O buffers in size")
+        self.copy_stream = torch.cuda.Stream(device=pool.device)
+
+    def bytes_per_step(self):
+        return self.pool.io_in.numel(), self.pool.io_out.numel()
+
+    def run(self, n: int):
+        """Enqueue n pipelined decode steps on the current stream (and the copy stream)."""
+        pool, x = self.pool, self.copy_stream
+        comp = torch.cuda.current_stream(pool.device)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        done, copied_in, copied_out = [None] * n, [None] * n, [None] * n
+        x.wait_stream(comp)
+
+        def copy_in(i):
+            with torch.cuda.stream(x):
+                if i >= 2:
+                    x.wait_event(done[i - 2])
+                pool._io[i % 2][0].copy_(self.host_in[i % len(self.host_in)].view(torch.uint8).view(-1),
+                                         non_blocking=True)
+                copied_in[i] = ev()
+                copied_in[i].record(x)
+
+        def copy_out(i):
+            with torch.cuda.stream(x):
+                x.wait_event(done[i])
+                self.host_out[i % len(self.host_out)].view(torch.uint8).view(-1).copy_(
+                    pool._io[i % 2][2], non_blocking=True)
+                copied_out[i] = ev()
+                copied_out[i].record(x)
+
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            comp.wait_event(copied_in[i])
+            if i >= 2:
+                comp.wait_event(copied_out[i - 2])
+            pool.io_slot(i % 2)
+            pool.step(validate=self.validate, stream=comp)
+            done[i] = ev()
+            done[i].record(comp)
+            if i >= 1:
+                copy_out(i - 1)
+        copy_out(n - 1)
+        comp.wait_stream(x)
+        pool.io_slot(0)
+
+
+def admission_cap(budget_bytes: int, context: int, *, Hkv: int, D: int, page_size: int,
+                  fp8: bool):
+    """Requests of `context` tokens a one-layer KV pool of `budget_bytes` admits.
+
+    A page holds K and V of page_size tokens for every kv head: 2*Hkv*page_size*D
+    elements of 1 byte (e4m3) or 2 (bf16).  The pool has floor(budget / page
+    bytes) pages and a request needs ceil(context / page_size) of them.
+    Returns (pages in the pool, pages per request, requests admitted).
+    """
+    page_bytes = 2 * Hkv * page_size * D * (1 if fp8 else 2)
+    pages = budget_bytes // page_bytes
+    per_request = -(-context // page_size)
+    return pages, per_request, (pages // per_request if per_request else 0)
