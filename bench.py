@@ -718,6 +718,27 @@ def validation_overhead(g_val, g_noval, pairs: int, replays: int):
             "step_us_with": 1e3 * statistics.median(tv), "step_us_without": 1e3 * statistics.median(tn)}
 
 
+def time_attention_b2b(pool, launches: int, reps: int = 5):
+    """The attention launch's average duration: `launches` back-to-back launches
+    on the current stream (same inputs, KV far larger than L2) between two
+    events, median over `reps` rounds.  Each launch's grid set-up overlaps the
+    previous launch's tail, as in the decode step, where attention is the
+    write + check kernel's programmatic dependent."""
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        pool.attend(use_mask=True, stream=s)
+    t = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(launches):
+            pool.attend(use_mask=True, stream=s)
+        b.record(s)
+        torch.cuda.synchronize()
+        t.append(a.elapsed_time(b) / launches)
+    return statistics.median(t)
+
+
 def time_attention_sequence(pool, staged, nsteps: int):
     """Attention launches of decode steps 0..nsteps-1, each timed with events on
     its stream after that step's inputs were staged and its write + check ran;
@@ -788,16 +809,21 @@ def measure_fp8(wl, args, world, local, headline: bool):
             ms_step = time_graph(g_seq, reps, 1) / seq_steps
         barrier(world)
         ms_step = max_over_ranks(ms_step, world)
-        # the attention launch alone, with events between the launches on their
-        # stream: at decode step 0, or over every step of a growing workload
+        # the attention launch alone: its average duration over back-to-back
+        # launches at decode step 0 (the roofline's), and each launch timed on
+        # its own between the step's launches (at step 0, or over every step
+        # of a growing workload), which adds the launch's own latency
         if staged is None:
             pool.set_step(0)
-            _, attn_ms, app_ms = time_steps(pool, max(args.steps // 4, 20), 3)
-            abytes = attention_bytes(wl, 0, True)
+            _, single_ms, app_ms = time_steps(pool, max(args.steps // 4, 20), 3)
+            single_bytes = attention_bytes(wl, 0, True)
         else:
-            attn_ms, app_ms = time_attention_sequence(pool, staged, seq_steps)
-            abytes = statistics.mean(attention_bytes(wl, s_, True) for s_ in range(seq_steps))
+            single_ms, app_ms = time_attention_sequence(pool, staged, seq_steps)
+            single_bytes = statistics.mean(attention_bytes(wl, s_, True) for s_ in range(seq_steps))
             pool.set_step(0)
+            pool.append_check()
+        attn_ms = time_attention_b2b(pool, 20)
+        abytes = attention_bytes(wl, 0, True)
         val = validation_overhead(g_step, g_noval, args.val_pairs, args.val_replays)
         status = fpk.fpk_decode_status(pool.workspace)
         if headline:
@@ -809,6 +835,11 @@ def measure_fp8(wl, args, world, local, headline: bool):
         "step_launch": ("one CUDA graph per step" if g_seq is None
                         else f"all {seq_steps} decode steps as one CUDA graph (inputs staged on the device)"),
         "attn_us": attn_ms * 1e3, "append_and_check_us": app_ms * 1e3,
+        "attn_timing": "average over 20 back-to-back launches at decode step 0 (median of 5 rounds)",
+        "attn_us_single_launch": single_ms * 1e3,
+        "single_launch_gbs": single_bytes / (single_ms * 1e-3) / 1e9,
+        "single_launch_timing": ("each launch between two events, after the step's write + check launch"
+                                 + (f", mean over all {seq_steps} steps" if staged is not None else "")),
         "attn_tokens_per_s": live * world / (attn_ms * 1e-3),
         "roofline": roofline(abytes, attn_ms, wl.name, peak, peak_kind),
         "validation_overhead_pct": val["median_pct"], "validation_overhead": val,
@@ -827,7 +858,8 @@ def measure_fp8(wl, args, world, local, headline: bool):
         pool.num_splits = 0
         pool.workspace = torch.zeros(max(256, fpk.fpk_decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.D, 0)),
                                      dtype=torch.uint8, device=dev)
-        _, a_auto, _ = time_steps(pool, 20, 3)
+        pool.append_check()
+        a_auto = time_attention_b2b(pool, 20)
         res["attn_us_auto_splits"] = a_auto * 1e3
         res["roofline_auto_splits_frac"] = attention_bytes(wl, 0, True) / (a_auto * 1e-3) / 1e9 / peak
     del pool
@@ -968,7 +1000,9 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 cache; f16 MMA, fp32 softmax",
         "data": "synthetic", "config": workload_config(wl),
         "roofline": m["roofline"],
-        "fp8": {"attn_us": m["attn_us"], "append_and_check_us": m["append_and_check_us"],
+        "fp8": {"attn_us": m["attn_us"], "attn_timing": m["attn_timing"],
+                "attn_us_single_launch": m["attn_us_single_launch"],
+                "append_and_check_us": m["append_and_check_us"],
                 "attn_tokens_per_s": m["attn_tokens_per_s"], "attn_gbs": m["roofline"]["achieved"],
                 "step_launch": m["step_launch"],
                 "validation_overhead_pct": m["validation_overhead_pct"],
@@ -989,12 +1023,15 @@ def main():
         p16.set_step(0)
         p16.count_aborts = False
         n16 = max(args.steps // 4, 20)
-        _, a16, _ = time_steps(p16, n16, args.warmup)
+        _, a16_single, _ = time_steps(p16, n16, args.warmup)
+        p16.append_check()
+        a16 = time_attention_b2b(p16, 20)
         g16 = capture_step(p16, True)
         t16 = time_graph(g16, n16, args.warmup) * n16
         b16 = attention_bytes(wl, 0, False)
         out["bf16"] = {"value": live * world / (t16 / n16 * 1e-3), "ms_per_step": t16 / n16,
-                       "attn_us": a16 * 1e3, "attn_gbs": b16 / (a16 * 1e-3) / 1e9,
+                       "attn_us": a16 * 1e3, "attn_us_single_launch": a16_single * 1e3,
+                       "attn_gbs": b16 / (a16 * 1e-3) / 1e9,
                        "attn_frac": b16 / (a16 * 1e-3) / 1e9 / peak,
                        "fp8_over_bf16_step": (t16 / n16) / ms_step,
                        "traffic": read_profile_traffic(wl.name, "bf16")}

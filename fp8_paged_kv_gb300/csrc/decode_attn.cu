@@ -234,6 +234,41 @@ __device__ __forceinline__ int token_of_row(int i) {
   return 4 * ((i & 7) >> 1) + (i & 1) + 2 * (i >> 3);
 }
 
+// The smallest common split size (in tiles) whose split count over the
+// batch's non-empty (request, kv head) segments fits the CTAs: every thread
+// counts the splits for one candidate between ceil(T / CTAs) and
+// ceil(T / (CTAs - segments)) (the last always fits: each segment's rounding
+// adds at most one split); a block min picks the smallest that fits.  A
+// segment's tile count fits in 32 bits, and so do the candidates that matter
+// (larger ones are clamped: they give one split per segment).  Called by
+// every thread of the CTA; kept out of line so that launches that never take
+// this partition do not carry its code in their prologue (measured on GB300:
+// inlined, it slowed small single launches by about 2 us).
+__device__ __noinline__ int64_t tightest_split_size(const AttnArgs& a, int64_t T, int nctas, int64_t segs,
+                                                    int64_t* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t hi = (T + (nctas - segs) - 1) / (nctas - segs);
+  const int64_t lo = T > nctas ? (T + nctas - 1) / nctas : 1;
+  const int64_t cand = lo + (hi - lo) * tid / (kThreads - 1);
+  const uint32_t c32 = static_cast<uint32_t>(min(cand, static_cast<int64_t>(0x7fffffff)));
+  int64_t cnt = 0;
+  for (int r = 0; r < a.B; ++r) {
+    const uint32_t n = static_cast<uint32_t>(tiles_of(a, r));
+    cnt += (n + c32 - 1u) / c32;
+  }
+  cnt *= a.Hkv;
+  int64_t best = cnt <= nctas ? cand : hi;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if (lane == 0) s_warp[warp] = best;
+  __syncthreads();
+  int64_t c = s_warp[0];
+#pragma unroll
+  for (int i = 1; i < kThreads / 32; ++i) c = min(c, s_warp[i]);
+  __syncthreads();  // s_warp is reused by the caller
+  return c;
+}
+
 template <bool kFp8, bool kDeep>
 __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const AttnArgs a) {
   using C = Cfg<kFp8, kDeep>;
@@ -261,6 +296,16 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   const int w = blockIdx.x;
   const unsigned kFull = 0xffffffffu;
 
+  // barriers: stage s is full0 + 8 s (filled) and empty0 + 8 s (consumed),
+  // then the merge barriers
+  const uint32_t full0 = smem_addr(bars);
+  const uint32_t empty0 = full0 + 8 * C::kStages;
+  const uint32_t merge_free = full0 + 16 * C::kStages;
+  const uint32_t cbar = merge_free + 8;  // consumer-warp barrier of the split-segment combine
+  // the two-slot merge of a piece: warps 2, 3 have filled slots 0, 1 (mrg0);
+  // warps 0, 1 have read them (mrg1); warps 0, 1 have filled them (mrg2).
+  // The four-slot merge: every warp has filled its slot (mrg4).
+  const uint32_t mrg0 = cbar + 8, mrg1 = cbar + 16, mrg2 = cbar + 24, mrg4 = cbar + 32;
   // ---- prologue: total tiles and this CTA's start (block scan over requests)
   const int chunk = (a.B + kThreads - 1) / kThreads;
   const int rb = tid * chunk;
@@ -322,16 +367,17 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   }
   // Segment-aligned partition (automatic count, lengths not all equal, at
   // most a third as many segments as CTAs): every non-empty segment is cut
-  // into splits of csz tiles (its last one shorter), csz = ceil(T / (CTAs -
-  // segments)), which keeps the count below the CTAs: one split per CTA, none
-  // straddling two segments, none more than half above T / CTAs.  (Measured
-  // on GB300 with 8192-token-scale mixed lengths: up to a third of the CTAs
-  // it gains 2-22 %; at half of them the larger splits lose up to 27 %.)
+  // into splits of csz tiles (its last one shorter), csz the smallest size
+  // whose split count fits the CTAs (at most ceil(T / (CTAs - segments))):
+  // one split per CTA, none straddling two segments, none more than half
+  // above T / CTAs.  (Measured on GB300 with 8192-token-scale mixed lengths:
+  // up to a third of the CTAs it gains 2-22 %; at half of them, with
+  // ceil(T / (CTAs - segments)), the larger splits lost up to 27 %.)
   const int64_t segs_nz = static_cast<int64_t>(nz_all) * a.Hkv;
   const bool aligned = a.auto_split && nz_all > 0 && tmin_all != tmax_all && 3 * segs_nz <= nctas;
   int64_t csz = 1, excl_splits = 0, mine_splits = 0;
   if (aligned) {
-    csz = (T + (nctas - segs_nz) - 1) / (nctas - segs_nz);
+    csz = tightest_split_size(a, T, nctas, segs_nz, s_warp_splits);
     for (int r = rb; r < re; ++r) {
       const int n = tiles_of(a, r);
       mine_splits += static_cast<int64_t>(a.Hkv) * ((n + csz - 1) / csz);
@@ -406,15 +452,6 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       base += span;
     }
   }
-  // barriers
-  const uint32_t full0 = smem_addr(bars);
-  const uint32_t empty0 = full0 + 8 * C::kStages;
-  const uint32_t merge_free = full0 + 16 * C::kStages;
-  const uint32_t cbar = merge_free + 8;  // consumer-warp barrier of the split-segment combine
-  // the two-slot merge of a piece: warps 2, 3 have filled slots 0, 1 (mrg0);
-  // warps 0, 1 have read them (mrg1); warps 0, 1 have filled them (mrg2).
-  // The four-slot merge: every warp has filled its slot (mrg4).
-  const uint32_t mrg0 = cbar + 8, mrg1 = cbar + 16, mrg2 = cbar + 24, mrg4 = cbar + 32;
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -683,17 +720,29 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
         acc0 = make_float4(acc0.x * r0, acc0.y * r0, acc0.z * r0, acc0.w * r0);
         acc1 = make_float4(acc1.x * r1, acc1.y * r1, acc1.z * r1, acc1.w * r1);
       }
-#pragma unroll 2
-      for (int i = 0; i < nc; ++i) {
-        const float4* po = reinterpret_cast<const float4*>(a.part_o + slot_of(c0 + i) * a.G * kDim);
-        const float4 v0 = __ldcg(po + hh0 * (kDim / 4) + d4);
-        const float4 v1 = __ldcg(po + hh1 * (kDim / 4) + d4);
-        const float f0 = s_w[i * kGroupMax + hh0].x;
-        const float f1 = s_w[i * kGroupMax + hh1].x;
-        acc0 = make_float4(fmaf(v0.x, f0, acc0.x), fmaf(v0.y, f0, acc0.y), fmaf(v0.z, f0, acc0.z),
-                           fmaf(v0.w, f0, acc0.w));
-        acc1 = make_float4(fmaf(v1.x, f1, acc1.x), fmaf(v1.y, f1, acc1.y), fmaf(v1.z, f1, acc1.z),
-                           fmaf(v1.w, f1, acc1.w));
+      // the slots' loads are issued four at a time, all before their FMAs:
+      // the partials sit in L2, and one slot per round trip made the combine
+      // of 16 partials eight dependent L2 round trips
+      for (int i0 = 0; i0 < nc; i0 += 4) {
+        float4 v0[4], v1[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = min(i0 + j, nc - 1);  // past the end: a repeated load, not used
+          const float4* po = reinterpret_cast<const float4*>(a.part_o + slot_of(c0 + i) * a.G * kDim);
+          v0[j] = __ldcg(po + hh0 * (kDim / 4) + d4);
+          v1[j] = __ldcg(po + hh1 * (kDim / 4) + d4);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (i0 + j < nc) {
+            const float f0 = s_w[(i0 + j) * kGroupMax + hh0].x;
+            const float f1 = s_w[(i0 + j) * kGroupMax + hh1].x;
+            acc0 = make_float4(fmaf(v0[j].x, f0, acc0.x), fmaf(v0[j].y, f0, acc0.y),
+                               fmaf(v0[j].z, f0, acc0.z), fmaf(v0[j].w, f0, acc0.w));
+            acc1 = make_float4(fmaf(v1[j].x, f1, acc1.x), fmaf(v1[j].y, f1, acc1.y),
+                               fmaf(v1[j].z, f1, acc1.z), fmaf(v1[j].w, f1, acc1.w));
+          }
+        }
       }
       // every thread is done with this chunk's weights before the next overwrites them
       if (c0 + kChunk < n && !consumer_sync()) return false;
@@ -1379,7 +1428,12 @@ int attn_entry(const void* q, const void* kv_pool, const float* k_scale,
   const int wave = device_sm_count(dev) * per_sm;  // CTAs resident at once
   if (per_sm <= 0 || wave <= 0) return FPK_ECUDA;
   const int W = num_splits == 0 ? auto_splits(wave, B, Hkv) : num_splits;
-  const int ctas = W < wave ? W : wave;  // more splits than that: a CTA runs several in turn
+  // more splits than a wave: a CTA runs several in turn, as few as the wave
+  // allows (k = ceil(W / wave)), and no more CTAs are launched than that
+  // count needs -- an equal number of splits per CTA, each CTA with a larger
+  // share of the memory system
+  const int per_cta = (W + wave - 1) / wave;
+  const int ctas = W <= wave ? W : (W + per_cta - 1) / per_cta;
   const int G = Hq / Hkv;
   const WsLayout l = layout(B, Hkv, G, W);
   if (workspace_bytes < l.total) return FPK_ENOSPC;

@@ -311,11 +311,14 @@ size_t fpk_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
  *               per (request, kv head) (at most 16); when lengths
  *               differ and the non-empty (request, kv head) pairs number at
  *               most a third of a wave, each is cut into splits of one
- *               common tile count c = ceil(tiles / (wave - pairs)) (its last
- *               split shorter), one split per CTA.  With equal
- *               context lengths, num_splits = S * B * Hkv gives exactly S
- *               splits per (request, kv head).  At most one wave of CTAs is
- *               launched; beyond that a CTA runs several splits in turn.
+ *               common tile count c (its last split shorter): the smallest c
+ *               for which the splits number no more than a wave, one split
+ *               per CTA.  With equal context lengths, num_splits = S * B * Hkv
+ *               gives exactly S splits per (request, kv head).  At most one
+ *               wave of CTAs is launched; with more splits than that, each
+ *               CTA runs several consecutive splits in turn.  Every split's
+ *               partial and every combine order are fixed, so repeated calls
+ *               on the same inputs give identical bits.
  *   sm_scale  : softmax scale (1/sqrt(D) for standard attention).
  */
 int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* kv_pool,
