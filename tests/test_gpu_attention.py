@@ -143,10 +143,11 @@ def test_uneven_batch_of_whole_segment_size(fp8):
 
 @pytest.mark.parametrize("fp8", [True, False])
 @pytest.mark.parametrize("num_splits", [305, 1000, 2200])
-def test_claimed_splits(fp8, num_splits):
-    # more splits than CTAs (a wave is 304 on GB300) and a tile in every
-    # split: CTA i starts with split i and the rest are claimed at run time;
-    # splits straddle requests and kv heads, one request is aborted
+def test_more_splits_than_a_wave(fp8, num_splits):
+    # more splits than a wave of CTAs (304 on GB300), a tile in every split:
+    # each CTA runs an equal number of consecutive splits (k = ceil(W / wave),
+    # ceil(W / k) CTAs); splits straddle requests and kv heads, one request
+    # is aborted
     lens = [7000, 33, 0, 10250, 640, 5, 1500]
     wl = custom(77 + num_splits, B=len(lens), Hq=16, Hkv=2, ps=16, prompt_lens=lens, steps=0,
                 sigma=1.2, outlier_frac=0.02)
@@ -155,10 +156,10 @@ def test_claimed_splits(fp8, num_splits):
     abort = np.zeros(wl.B, np.uint8)
     abort[4] = 1
     out, lse, ro, rl = _run_case(wl, fp8, num_splits, abort=abort, use_mask=True)
-    assert_attention_close(out, lse, ro, rl, f"claimed splits={num_splits} fp8={fp8}")
+    assert_attention_close(out, lse, ro, rl, f"splits={num_splits} fp8={fp8}")
 
 
-@pytest.mark.parametrize("case", ["uniform", "uneven", "splits200", "splits4096", "claimed2000"])
+@pytest.mark.parametrize("case", ["uniform", "uneven", "splits200", "splits4096", "wave2000"])
 def test_repeated_launches_bit_identical(case):
     # the partition, each CTA's merge order and each segment's combine order
     # are fixed, whichever CTA arrives last: repeated launches must agree to
@@ -167,8 +168,8 @@ def test_repeated_launches_bit_identical(case):
         lens, ns = [700] * 30, 0
     elif case == "uneven":
         lens, ns = list(rng_for(85, "lens").integers(1, 1400, size=30)), 0
-    elif case == "claimed2000":
-        # claimed at run time: which CTA runs which split varies, the bits do not
+    elif case == "wave2000":
+        # more splits than a wave, a tile in every split: 7 consecutive splits per CTA
         lens, ns = list(rng_for(86, "lens").integers(2000, 6000, size=12)), 2000
     else:
         lens, ns = list(rng_for(86, "lens").integers(1, 3000, size=12)), int(case[6:])
