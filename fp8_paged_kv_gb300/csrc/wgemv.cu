@@ -162,8 +162,262 @@ struct GemvArgs {
   const float* rscales;     // e4m3: fp32 [N]
   float* y;                 // fp32 [B][N]
   int B, N, K;
+  int kc;                   // k per CTA (a multiple of 128, at most kKChunk)
   int atomic;               // several K chunks add into y
 };
+
+// Asynchronous 16-byte global -> shared copy (Ampere-style cp.async, L2 only).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+// f16x2 of two nibbles of v (bits 0..3 and 16..19 when kHigh is false, bits
+// 4..7 and 20..23 when true) by placing them in the mantissa of 1024.0
+// (0x6400: the unit in the last place is 1), then subtracting the bias:
+// 1024 + 8 gives n - 8; for the upper nibbles, 1024 + 16 n - (1024 + 128)
+// gives 16 (n - 8) -- every step exact in f16.
+// mask and magic are passed in registers so that the and-or is one LOP3.
+__device__ __forceinline__ uint32_t w4_pair_to_f16x2(uint32_t v, uint32_t mask, uint32_t magic, uint32_t bias) {
+  uint32_t b;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(b) : "r"(v), "r"(mask), "r"(magic));  // (v & mask) | magic
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&b), *reinterpret_cast<const __half2*>(&bias));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// One CTA: 8 warps x one 16-row slice each, over one K chunk of up to 2048.
+// Each lane streams its own 16-byte words of the warp's slice groups into a
+// shared-memory ring with cp.async (in the slice layout a lane reads back only
+// the bytes it copied itself, so no cross-lane barrier is needed), keeping
+// kRing - 1 groups in flight without holding them in registers.  The chunk's
+// activations are staged once per CTA as f16: row b scaled by a power of two
+// 2^e_b that takes its largest |x| into [2^14, 2^15), which is exact for every
+// value not below 2^-14 after scaling (f16 has more mantissa bits than bf16);
+// for INT4 the activations at k = 2, 3 (mod 4) are staged divided by 16,
+// because the weights there come out of the nibble trick multiplied by 16.
+// kNT n8 tiles of batch columns (B <= 8 kNT); only the B real rows are staged.
+// kRing groups of ring per warp (kRing - 1 in flight).
+template <bool kW4, int kNT, int kRing>
+__global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
+  extern __shared__ __align__(16) uint8_t gsm[];
+  constexpr int kSliceBytes = kW4 ? kW4SliceBytes : kW8SliceBytes;
+  constexpr int kRingBytesPerWarp = kRing * kSliceBytes;
+  constexpr int kVec = kSliceBytes / 512;                 // 16-byte words per lane per group
+  __shared__ float s_unscale[8 * kNT];                    // 2^-e_b per staged row
+  __shared__ uint16_t s_gscale[kGemvWarps * 16][kKChunk / kGroupK];  // INT4 group scales of the CTA's rows
+  const int G = a.K / kGroupK;
+  const int k0 = blockIdx.y * a.kc;
+  const int kc = min(a.kc, a.K - k0);
+  const int ng = kc / kGroupK;
+  const int g0 = k0 / kGroupK;
+  const int xstride = kc + kXPad;
+  const int rows = min(a.B, 8 * kNT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slice = blockIdx.x * kGemvWarps + warp;
+  const bool has_slice = slice < a.N / 16;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(gsm + kGemvWarps * kRingBytesPerWarp);
+  // ---- this warp's weight stream starts first
+  const uint8_t* wp = a.codes + (static_cast<int64_t>(has_slice ? slice : 0) * G + g0) * kSliceBytes + 16 * lane;
+  const uint32_t ring = smem_addr(gsm + warp * kRingBytesPerWarp) + 16 * lane;
+  auto issue = [&](int gi) {
+    if (has_slice && gi < ng) {
+#pragma unroll
+      for (int i = 0; i < kVec; ++i)
+        cp_async16(ring + (gi % kRing) * kSliceBytes + 512 * i, wp + static_cast<int64_t>(gi) * kSliceBytes + 512 * i);
+    }
+    cp_async_commit();  // one group per step, empty or not: the wait counts stay uniform
+  };
+#pragma unroll
+  for (int gi = 0; gi < kRing - 1; ++gi) issue(gi);
+  // ---- the CTA's INT4 group scales for this chunk (ng per row; a row's run
+  // of scales is not 16-byte aligned in general, so element by element)
+  if (kW4) {
+    for (int i = threadIdx.x; i < kGemvWarps * 16 * ng; i += kGemvThreads) {
+      const int rrow = i / ng, gi = i - rrow * ng;
+      const int row = blockIdx.x * kGemvWarps * 16 + rrow;
+      s_gscale[rrow][gi] = row < a.N ? __ldg(a.gscales + static_cast<int64_t>(row) * G + g0 + gi) : 0;
+    }
+  }
+  // ---- stage the chunk's activations: every thread takes the 8 values
+  // 8 tid .. 8 tid + 7 of each row (kc / 8 <= kGemvThreads); the loads of all
+  // rows go out before any reduction, then the row's largest |x| (bit
+  // patterns, non-finite as 0) per warp, then the scaled f16 copy
+  __shared__ uint32_t s_wmax[8 * kNT][kGemvWarps];
+  const bool has_item = static_cast<int>(threadIdx.x) < kc / 8;
+  {
+    uint32_t m2[8 * kNT];
+#pragma unroll
+    for (int b = 0; b < 8 * kNT; ++b) {
+      m2[b] = 0u;
+      if (b < rows && has_item) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0) + threadIdx.x);
+        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t u = ws[q] & 0x7FFF7FFFu;
+          u &= __vcmpltu2(u, 0x7F807F80u);
+          m2[b] = __vmaxu2(m2[b], u);
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 8 * kNT; ++b) {
+      if (b < rows) {
+        const uint32_t mb = __reduce_max_sync(0xffffffffu, max(m2[b] & 0xFFFFu, m2[b] >> 16));
+        if (lane == 0) s_wmax[b][warp] = mb;
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < 8 * kNT; ++b) {
+    if (b < rows) {
+      uint32_t mb = 0u;
+#pragma unroll
+      for (int w2 = 0; w2 < kGemvWarps; ++w2) mb = max(mb, s_wmax[b][w2]);
+      const int e = mb == 0 ? 0 : min(max(14 - ilogbf(__uint_as_float(mb << 16)), -126), 126);
+      const float sc = __int_as_float((127 + e) << 23);
+      if (threadIdx.x == 0) s_unscale[b] = __int_as_float((127 - e) << 23);
+      if (has_item) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0) + threadIdx.x);
+        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // elements 8 tid + 2q, + 1: k mod 4 = 2q mod 4, 2q mod 4 + 1
+          const float f = (kW4 && (q & 1)) ? sc * 0.0625f : sc;
+          o[q] = pack_f16x2(__uint_as_float(ws[q] << 16) * f, __uint_as_float(ws[q] & 0xFFFF0000u) * f);
+        }
+        *reinterpret_cast<uint4*>(xs + b * xstride + 8 * threadIdx.x) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+  // one zeroed row after the staged ones: the B operand of absent batch columns
+  for (int i = threadIdx.x; i < (kc + kXPad) / 8; i += kGemvThreads)
+    *reinterpret_cast<uint4*>(xs + rows * xstride + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  if (!has_slice) {
+    cp_async_wait<0>();
+    return;
+  }
+  const int rr = lane >> 2, t = lane & 3;
+  const int row0 = 16 * slice + rr, row1 = row0 + 8;
+  const int lrow0 = 16 * warp + rr, lrow1 = lrow0 + 8;  // rows within the CTA's scale table
+
+  float acc[kNT][4];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  // batch column 8 nt + rr of the B operand: columns past B read the zero row
+  const uint16_t* xcol[kNT];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) xcol[nt] = xs + min(8 * nt + rr, rows) * xstride + 4 * t;
+  // nibble masks, the f16 magic 1024 and the biases, in registers
+  const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
+  const uint32_t blo = 0x64086408u, bhi = 0x64806480u;  // 1032, 1152
+  const uint16_t* gsc0 = &s_gscale[lrow0][0];
+  const uint16_t* gsc1 = &s_gscale[lrow1][0];
+
+  // ring bookkeeping by running offsets: group gi is read from slot rd; the
+  // group kRing - 1 ahead is written into the slot the previous group left
+  // (whose words are in registers by now)
+  const uint8_t* ring_ld = gsm + warp * kRingBytesPerWarp + 16 * lane;
+  const uint8_t* gsrc = wp + static_cast<int64_t>(kRing - 1) * kSliceBytes;
+  uint32_t rd = 0, wr = (kRing - 1) * kSliceBytes;
+  for (int gi = 0; gi < ng; ++gi) {
+    cp_async_wait<kRing - 2>();  // group gi has landed (this lane's words)
+    uint4 cur[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) cur[i] = *reinterpret_cast<const uint4*>(ring_ld + rd + 512 * i);
+    if (gi + kRing - 1 < ng) {
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) cp_async16(ring + wr + 512 * i, gsrc + 512 * i);
+    }
+    cp_async_commit();
+    gsrc += kSliceBytes;
+    wr = rd;
+    rd = rd + kSliceBytes == kRingBytesPerWarp ? 0u : rd + kSliceBytes;
+    // two accumulator chains per group (even and odd steps)
+    float ae[kNT][4], ao[kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      ae[nt][0] = ae[nt][1] = ae[nt][2] = ae[nt][3] = 0.f;
+      ao[nt][0] = ao[nt][1] = ao[nt][2] = ao[nt][3] = 0.f;
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t af[4];
+      if (kW4) {
+        // cur[0]: row0's words, cur[1]: row1's; word s/2; odd steps use the
+        // nibbles 8 bits up
+        const uint32_t v0 = s < 2 ? cur[0].x : s < 4 ? cur[0].y : s < 6 ? cur[0].z : cur[0].w;
+        const uint32_t v1 = s < 2 ? cur[1].x : s < 4 ? cur[1].y : s < 6 ? cur[1].z : cur[1].w;
+        const uint32_t u0 = (s & 1) ? v0 >> 8 : v0;
+        const uint32_t u1 = (s & 1) ? v1 >> 8 : v1;
+        af[0] = w4_pair_to_f16x2(u0, mlo, magic, blo);  // row0, j0 j1: n - 8
+        af[1] = w4_pair_to_f16x2(u1, mlo, magic, blo);  // row1, j0 j1
+        af[2] = w4_pair_to_f16x2(u0, mhi, magic, bhi);  // row0, j2 j3: 16 (n - 8)
+        af[3] = w4_pair_to_f16x2(u1, mhi, magic, bhi);  // row1, j2 j3
+      } else {
+        // cur[0], cur[1]: row0 steps 0-3, 4-7; cur[2], cur[3]: row1; word = step
+        const uint4& r0 = cur[s >> 2];
+        const uint4& r1 = cur[2 + (s >> 2)];
+        const uint32_t c0 = (s & 3) == 0 ? r0.x : (s & 3) == 1 ? r0.y : (s & 3) == 2 ? r0.z : r0.w;
+        const uint32_t c1 = (s & 3) == 0 ? r1.x : (s & 3) == 1 ? r1.y : (s & 3) == 2 ? r1.z : r1.w;
+        af[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(c0 & 0xFFFFu));
+        af[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(c1 & 0xFFFFu));
+        af[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(c0 >> 16));
+        af[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(c1 >> 16));
+      }
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        const uint2 bv = *reinterpret_cast<const uint2*>(xcol[nt] + kGroupK * gi + 16 * s);
+        if (s & 1) mma_f16(ao[nt], af, bv.x, bv.y);
+        else mma_f16(ae[nt], af, bv.x, bv.y);
+      }
+    }
+    if (kW4) {
+      const float s0 = bf16_bits_to_float(gsc0[gi]);
+      const float s1 = bf16_bits_to_float(gsc1[gi]);
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        acc[nt][0] = fmaf(ae[nt][0] + ao[nt][0], s0, acc[nt][0]);
+        acc[nt][1] = fmaf(ae[nt][1] + ao[nt][1], s0, acc[nt][1]);
+        acc[nt][2] = fmaf(ae[nt][2] + ao[nt][2], s1, acc[nt][2]);
+        acc[nt][3] = fmaf(ae[nt][3] + ao[nt][3], s1, acc[nt][3]);
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] += ae[nt][e] + ao[nt][e];
+    }
+  }
+  cp_async_wait<0>();
+  float r0s = 1.f, r1s = 1.f;
+  if (!kW4) {
+    r0s = __ldg(a.rscales + row0);
+    r1s = __ldg(a.rscales + row1);
+  }
+  // accumulator (row, column): c0 (row0, 2t), c1 (row0, 2t+1), c2 (row1, 2t), c3 (row1, 2t+1)
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int b = 8 * nt + 2 * t + (e & 1);
+      const int row = e < 2 ? row0 : row1;
+      if (b < a.B) {
+        float* yp = a.y + static_cast<int64_t>(b) * a.N + row;
+        const float v = acc[nt][e] * (e < 2 ? r0s : r1s) * s_unscale[b];
+        if (a.atomic) atomicAdd(yp, v);
+        else *yp = v;
+      }
+    }
+  }
+}
 
 // bf16x2 of two excess-8 nibbles (bits 0..3 and 16..19 of v): 128 + nibble is
 // exact in bf16 (one unit in the last place at 128), so subtracting 136 gives
@@ -182,17 +436,21 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t c) {
   return pack_bf16x2(f.x, f.y);
 }
 
-// One CTA: 8 warps x one 16-row slice each, over one K chunk.  kNT n8 tiles of
-// batch columns (B <= 8 * kNT).  kPF groups of weights are in flight per lane.
+// Register-streaming variant for batches of 5..16 tokens, where the staged
+// activations leave too little shared memory for the landing rings: one CTA
+// of 8 warps x one 16-row slice each over one K chunk of kKChunk, kPF groups
+// of weights in flight per lane in registers, activations staged as the bf16
+// values they are (8 kNT rows, zeros past B), bf16 weights from the nibbles.
+// kNT n8 tiles of batch columns (B <= 8 * kNT).
 template <bool kW4, int kNT>
-__global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kGemvThreads) wgemv_regs_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) uint16_t xs[];  // [8 * kNT][kc + kXPad]
   constexpr int kSliceBytes = kW4 ? kW4SliceBytes : kW8SliceBytes;
   constexpr int kVec = kW4 ? 2 : 4;  // 16-byte words per lane per group
   constexpr int kPF = kW4 ? 4 : 2;
   const int G = a.K / kGroupK;
-  const int k0 = blockIdx.y * kKChunk;
-  const int kc = min(kKChunk, a.K - k0);
+  const int k0 = blockIdx.y * a.kc;
+  const int kc = min(a.kc, a.K - k0);
   const int ng = kc / kGroupK;
   const int xstride = kc + kXPad;
   // ---- stage the activations of this chunk (rows past B are zero)
@@ -330,15 +588,39 @@ int gemv_entry(const void* x, const uint8_t* codes, const void* gscales, const f
   a.B = B;
   a.N = N;
   a.K = K;
-  const int chunks = (K + kKChunk - 1) / kKChunk;
+  // Kernel and ring depth by batch: in the landing-ring kernel the staged
+  // activations (B + 1 rows of f16) and the rings share the shared memory,
+  // three CTAs (24 warps) per SM at 1 and 3-4 tokens, two at 2; beyond 4
+  // tokens too little is left for the rings, and the register-streaming
+  // kernel is faster.  (Smaller K chunks to keep three CTAs were measured
+  // slower: each CTA's staging and ring fill then cover too few groups.)
+  const int kc = K < kKChunk ? K : kKChunk;
+  a.kc = kc;
+  const int chunks = (K + kc - 1) / kc;
   a.atomic = chunks > 1;
   if (a.atomic && cudaMemsetAsync(y, 0, sizeof(float) * B * static_cast<size_t>(N), s) != cudaSuccess)
     return FPK_ECUDA;
   const int nt = B <= 8 ? 1 : 2;
-  const int kc = K < kKChunk ? K : kKChunk;
-  const size_t smem = static_cast<size_t>(8 * nt) * (kc + kXPad) * sizeof(uint16_t);
   const dim3 grid((N / 16 + kGemvWarps - 1) / kGemvWarps, chunks);
-  auto kern = nt == 1 ? wgemv_kernel<kW4, 1> : wgemv_kernel<kW4, 2>;
+  if (B > 4) {
+    // 5..16 tokens: the register-streaming kernel (measured faster there:
+    // INT4 at 28672 x 8192, 8 tokens 43 against 50 us, 16 tokens 53 against 72 us)
+    const size_t rsm = static_cast<size_t>(8 * nt) * (kc + kXPad) * sizeof(uint16_t);
+    void (*rk)(GemvArgs) = nt == 1 ? wgemv_regs_kernel<kW4, 1> : wgemv_regs_kernel<kW4, 2>;
+    if (rsm > 48 * 1024 &&
+        cudaFuncSetAttribute(rk, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(rsm)) != cudaSuccess)
+      return FPK_ECUDA;
+    rk<<<grid, kGemvThreads, rsm, s>>>(a);
+    return checked_launch_status();
+  }
+  // 1..4 tokens: the landing-ring kernel; ring groups per warp -- INT4 8
+  // (B <= 2) or 6, e4m3 4 or 3
+  const int ring = kW4 ? (B <= 2 ? 8 : 6) : (B <= 2 ? 4 : 3);
+  const size_t smem = static_cast<size_t>(kGemvWarps) * ring * (kW4 ? kW4SliceBytes : kW8SliceBytes) +
+                      static_cast<size_t>(B + 1) * (kc + kXPad) * sizeof(uint16_t);  // + the zero row
+  void (*kern)(GemvArgs);
+  if constexpr (kW4) kern = B <= 2 ? wgemv_kernel<true, 1, 8> : wgemv_kernel<true, 1, 6>;
+  else kern = B <= 2 ? wgemv_kernel<false, 1, 4> : wgemv_kernel<false, 1, 3>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return FPK_ECUDA;

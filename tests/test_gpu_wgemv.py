@@ -2,15 +2,22 @@
 e4m3 with a row scale as the comparison).
 
 Quantiser output (codes in the slice layout and scales) bit-exact against the
-oracle; y within a bound derived from the arithmetic.  The activations enter
-the tensor cores as the bf16 values they are and the weights as exact bf16
-(an INT4 code, or an e4m3 value), so every product is exact in fp32; the
-tensor cores sum 16 per step in fp32, a group's 8 steps are summed in fp32,
-scaled once, and the K/128 group sums (and the split-K chunks) are added in
-fp32: at most (8 + 1 + K/128 + 2) roundings of relative size 2^-24 (2^-23 if
-the tensor core truncates) on a sum bounded by sum_k |w x|:
+oracle; y within a bound derived from the arithmetic.  Up to 4 tokens the
+weights enter the tensor cores as exact f16 (an INT4 code, 16 times one, or an
+e4m3 value) and the activations as f16 copies of the bf16 values times a power
+of two (per token and K chunk, largest |x| taken into [2^14, 2^15); for INT4
+every other pair divided by 16), exact except for values that fall below 2^-14
+after scaling, which round to f16 subnormals with an error under 2^-25 of the
+scaled unit, i.e. 2^-35 max|x| before scaling; from 5 tokens on, both enter as
+exact bf16.  Every other product is exact in fp32.  The
+tensor cores sum 16 per step in fp32, a group's steps are summed in fp32 (two
+chains, then added), scaled once, and the K/128 group sums (and the split-K
+chunks) are added in fp32: at most (8 + 2 + K/128 + 2) roundings of relative
+size 2^-24 (2^-23 if the tensor core truncates) on a sum bounded by
+sum_k |w x|:
 |y - y_ref| <= 4 (16 + K/128) 2^-24 sum_k |w_k x_k|  (plus a 2^-30 max|x|
-sum_k |w_k| allowance for results near the bottom of the fp32 range).
+sum_k |w_k| allowance for the subnormal activations and for results near the
+bottom of the fp32 range).
 """
 import numpy as np
 import pytest
