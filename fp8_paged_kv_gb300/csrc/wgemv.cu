@@ -296,9 +296,6 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
       }
     }
   }
-  // one zeroed row after the staged ones: the B operand of absent batch columns
-  for (int i = threadIdx.x; i < (kc + kXPad) / 8; i += kGemvThreads)
-    *reinterpret_cast<uint4*>(xs + rows * xstride + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   if (!has_slice) {
     cp_async_wait<0>();
@@ -311,10 +308,12 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   float acc[kNT][4];
 #pragma unroll
   for (int nt = 0; nt < kNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-  // batch column 8 nt + rr of the B operand: columns past B read the zero row
+  // batch column 8 nt + rr of the B operand; columns past B repeat the last
+  // staged row: every output column of the MMA depends on its own B column
+  // only, and the columns past B are never written out
   const uint16_t* xcol[kNT];
 #pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) xcol[nt] = xs + min(8 * nt + rr, rows) * xstride + 4 * t;
+  for (int nt = 0; nt < kNT; ++nt) xcol[nt] = xs + min(8 * nt + rr, rows - 1) * xstride + 4 * t;
   // nibble masks, the f16 magic 1024 and the biases, in registers
   const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
   const uint32_t blo = 0x64086408u, bhi = 0x64806480u;  // 1032, 1152
@@ -589,11 +588,13 @@ int gemv_entry(const void* x, const uint8_t* codes, const void* gscales, const f
   a.N = N;
   a.K = K;
   // Kernel and ring depth by batch: in the landing-ring kernel the staged
-  // activations (B + 1 rows of f16) and the rings share the shared memory,
+  // activations (B rows of f16) and the rings share the shared memory,
   // three CTAs (24 warps) per SM at 1 and 3-4 tokens, two at 2; beyond 4
   // tokens too little is left for the rings, and the register-streaming
   // kernel is faster.  (Smaller K chunks to keep three CTAs were measured
-  // slower: each CTA's staging and ring fill then cover too few groups.)
+  // slower: each CTA's staging and ring fill then cover too few groups; so
+  // was summing the K chunks of a row block in a thread-block cluster instead
+  // of atomics into a zeroed y: 41.0 against 36.8 us at one token.)
   const int kc = K < kKChunk ? K : kKChunk;
   a.kc = kc;
   const int chunks = (K + kc - 1) / kc;
@@ -617,7 +618,7 @@ int gemv_entry(const void* x, const uint8_t* codes, const void* gscales, const f
   // (B <= 2) or 6, e4m3 4 or 3
   const int ring = kW4 ? (B <= 2 ? 8 : 6) : (B <= 2 ? 4 : 3);
   const size_t smem = static_cast<size_t>(kGemvWarps) * ring * (kW4 ? kW4SliceBytes : kW8SliceBytes) +
-                      static_cast<size_t>(B + 1) * (kc + kXPad) * sizeof(uint16_t);  // + the zero row
+                      static_cast<size_t>(B) * (kc + kXPad) * sizeof(uint16_t);
   void (*kern)(GemvArgs);
   if constexpr (kW4) kern = B <= 2 ? wgemv_kernel<true, 1, 8> : wgemv_kernel<true, 1, 6>;
   else kern = B <= 2 ? wgemv_kernel<false, 1, 4> : wgemv_kernel<false, 1, 3>;
