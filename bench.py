@@ -150,7 +150,7 @@ def measured_peaks():
 
 
 # the sources compiled into the attention kernel's translation unit
-KERNEL_SOURCES = ("decode_attn.cu", "common.cuh", "step_ops.cuh", "quant.cuh")
+KERNEL_SOURCES = ("decode_attn.cu", "attn_plan.cuh", "common.cuh", "step_ops.cuh", "quant.cuh")
 
 
 def _strip_comments(src: str) -> str:
@@ -824,6 +824,10 @@ def measure_fp8(wl, args, world, local, headline: bool):
             pool.append_check()
         attn_ms = time_attention_b2b(pool, 20)
         abytes = attention_bytes(wl, 0, True)
+        # the same launch on the tcgen05 tensor cores (fpk_paged_decode_attn_fp8_tc)
+        pool.tensor_cores = True
+        tc_ms = time_attention_b2b(pool, 20)
+        pool.tensor_cores = False
         val = validation_overhead(g_step, g_noval, args.val_pairs, args.val_replays)
         status = fpk.fpk_decode_status(pool.workspace)
         if headline:
@@ -842,6 +846,11 @@ def measure_fp8(wl, args, world, local, headline: bool):
                                  + (f", mean over all {seq_steps} steps" if staged is not None else "")),
         "attn_tokens_per_s": live * world / (attn_ms * 1e-3),
         "roofline": roofline(abytes, attn_ms, wl.name, peak, peak_kind),
+        "tensor_cores": {"attn_us": tc_ms * 1e3, "attn_gbs": abytes / (tc_ms * 1e-3) / 1e9,
+                         "frac": abytes / (tc_ms * 1e-3) / 1e9 / peak,
+                         "kernel": "paged_decode_tc_kernel: tcgen05.mma kind::f8f6f4 (q and p as four e4m3 "
+                                   "parts), accumulators in TMEM, K rows by tensor-map copies",
+                         "attn_timing": "average over 20 back-to-back launches at decode step 0 (median of 5 rounds)"},
         "validation_overhead_pct": val["median_pct"], "validation_overhead": val,
         "status_word": status, "clocks": clk.summary(), "live_requests": live})
     if wl.num_splits:
@@ -1008,7 +1017,7 @@ def main():
                 "validation_overhead_pct": m["validation_overhead_pct"],
                 "validation_overhead": m["validation_overhead"],
                 "algorithmic_bytes_per_attention": m["roofline"]["algorithmic_bytes"],
-                "status_word": m["status_word"]},
+                "status_word": m["status_word"], "tensor_cores": m["tensor_cores"]},
         # per timed step: the cache write + tag check launch and the attention
         # launch (the split combine runs inside the attention kernel)
         "gpu_launches": 2 * m["timed_steps"], "clocks": m["clocks"],

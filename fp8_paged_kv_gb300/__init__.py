@@ -55,6 +55,9 @@ SIGNATURES = {
     "fpk_paged_decode_attn_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
                                                  _SZ, _I32, _F, _I32, _I32, _I32, _I32, _I32, _I32,
                                                  _P]),
+    "fpk_paged_decode_attn_fp8_tc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P,
+                                                    _SZ, _I32, _F, _I32, _I32, _I32, _I32, _I32,
+                                                    _I32, _P]),
     "fpk_paged_decode_attn_bf16": (ctypes.c_int, [_P, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ,
                                                   _I32, _F, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "fpk_paged_decode_attn_fp8_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P,
@@ -264,6 +267,21 @@ def fpk_paged_decode_attn_fp8(q, kv_pool, k_scale, v_scale, page_table, seq_lens
         _ptr(lse, _F32, "lse", True), _ptr(workspace, _U8, "workspace"),
         workspace.numel(), num_splits, sm_scale, B, Hq, Hkv, D, page_size, num_pages,
         _stream(stream)), "fpk_paged_decode_attn_fp8")
+
+
+def fpk_paged_decode_attn_fp8_tc(q, kv_pool, k_scale, v_scale, page_table, seq_lens,
+                                 abort_mask, out, lse, workspace, *, Hkv, page_size, num_pages,
+                                 sm_scale, num_splits=0, stream=None):
+    """fpk_paged_decode_attn_fp8 on the tcgen05 tensor cores (same arguments)."""
+    B, Hq, D = q.shape
+    _check(load_library().fpk_paged_decode_attn_fp8_tc(
+        _ptr(q, _BF16_LIKE, "q"), _ptr(kv_pool, _U8, "kv_pool"),
+        _ptr(k_scale, _F32, "k_scale"), _ptr(v_scale, _F32, "v_scale"),
+        _ptr(page_table, _I32T, "page_table"), page_table.shape[1], _ptr(seq_lens, _I32T, "seq_lens"),
+        _ptr(abort_mask, _U8, "abort_mask", True), _ptr(out, _F32, "out"),
+        _ptr(lse, _F32, "lse", True), _ptr(workspace, _U8, "workspace"),
+        workspace.numel(), num_splits, sm_scale, B, Hq, Hkv, D, page_size, num_pages,
+        _stream(stream)), "fpk_paged_decode_attn_fp8_tc")
 
 
 def fpk_decode_step_fp8(k_new, v_new, kv_pool, k_scale, v_scale, page_table, seq_lens, live_tags,

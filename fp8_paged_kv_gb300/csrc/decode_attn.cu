@@ -47,36 +47,16 @@
 //   without a timeout is used after the prologue.
 #include <atomic>
 
+#include "attn_plan.cuh"
 #include "common.cuh"
 #include "step_ops.cuh"
 
 namespace fpk {
 namespace {
 
-constexpr int kTile = 16;        // tokens per tile
-constexpr int kDim = 128;        // head dimension
-constexpr int kGroupMax = 8;     // query heads per kv head (N of the MMA tile)
 constexpr int kMergeStride = 132;  // floats per head row of the merge buffer
 constexpr int kMergeBars = 6;      // merge_free, cbar, the three rounds of the two-slot merge, the four-slot one
 constexpr int64_t kInflightBudget = 26ll << 20;  // bytes of ring stages over the grid (see Cfg)
-// The automatic split count: one wave of CTAs, but no more than 16 splits per
-// (request, kv head) segment -- small batches then keep the one-level combine
-// and CTAs with enough tiles to cover their start-up.
-constexpr int kAutoSplitsPerSegment = 16;
-
-// The automatic split count of a batch whose segments all have one length
-// (seen on the device, from the context lengths): one whole segment per CTA
-// when the segments fill between 3/4 of the CTAs and all of them; with fewer
-// segments, the same number of splits for each (as many as the CTAs allow,
-// at most kAutoSplitsPerSegment), which puts every split boundary on a
-// segment boundary -- no split straddles two segments.  0: keep the count.
-__host__ __device__ __forceinline__ int64_t uniform_auto_splits(int64_t segs, int64_t nctas) {
-  if (segs <= 0 || segs > nctas) return 0;
-  if (4 * segs >= 3 * nctas) return segs;
-  int64_t m = nctas / segs;
-  if (m > kAutoSplitsPerSegment) m = kAutoSplitsPerSegment;
-  return segs * m;
-}
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 static_assert(kConsumerWarps * 32 == 128, "the split-segment combine gives each consumer thread one of the 128 dims");
@@ -140,12 +120,6 @@ struct AttnArgs {
   float sm_scale_log2;
 };
 
-struct Piece {
-  int r, h, t0, t1, n;
-  int s;       // split whose partial this piece produces
-  int64_t x0;  // global tile index of tile t0
-};
-
 // Slots of the members i0, i0 + stride, ... of one segment's partials: member
 // i is split w0 + i when every split owns tiles, else the owner of tile i.
 struct Members {
@@ -153,64 +127,6 @@ struct Members {
   int w0, i0, stride;
   bool dense;
 };
-
-struct Cursor {
-  int r, h, t, n;
-  int64_t x, remaining;
-  int split;  // >= 0: the CTA's one split of a segment-aligned partition
-};
-
-// Tiles of request r in the work list: its context length only.  The work
-// list is built before the abort mask may be read (the mask can come from the
-// kernel launched just before this one); pieces of aborted requests are
-// skipped after the dependency wait (is_aborted).
-__device__ __forceinline__ int tiles_of(const AttnArgs& a, int r) {
-  return tiles_of_request(a.seq_lens, nullptr, r, a.max_pages, a.page_size);
-}
-
-__device__ __forceinline__ bool is_aborted(const AttnArgs& a, int r) {
-  return a.abort_mask != nullptr && __ldcg(a.abort_mask + r) != 0;
-}
-
-// Worker w owns global tiles [floor(w T / W), floor((w+1) T / W)); the owner
-// of tile x is floor(((x + 1) W - 1) / T).  With W > T some workers own none.
-__device__ __forceinline__ int worker_of(int64_t x, int64_t T, int W) {
-  return static_cast<int>(((x + 1) * W - 1) / T);
-}
-
-// The next piece of a CTA's tile range: the longest run that stays inside one
-// (request, kv head) segment and one split.
-__device__ __forceinline__ bool next_piece(Cursor& c, const AttnArgs& a, int64_t T, int W, Piece& p) {
-  if (c.remaining <= 0) return false;
-  const int s = c.split >= 0 ? c.split : worker_of(c.x, T, W);
-  const int64_t split_end = c.split >= 0 ? c.x + c.remaining : (static_cast<int64_t>(s) + 1) * T / W;
-  int64_t take64 = c.n - c.t;
-  if (c.remaining < take64) take64 = c.remaining;
-  if (split_end - c.x < take64) take64 = split_end - c.x;
-  const int take = static_cast<int>(take64);
-  p.s = s;
-  p.r = c.r;
-  p.h = c.h;
-  p.t0 = c.t;
-  p.t1 = c.t + take;
-  p.n = c.n;
-  p.x0 = c.x;
-  c.remaining -= take;
-  c.x += take;
-  c.t += take;
-  if (c.remaining > 0 && c.t == c.n) {
-    c.t = 0;
-    if (++c.h == a.Hkv) {
-      c.h = 0;
-      do {
-        ++c.r;
-        c.n = c.r < a.B ? tiles_of(a, c.r) : 1;
-      } while (c.n == 0);
-      if (c.r >= a.B) c.remaining = 0;  // unreachable with consistent inputs
-    }
-  }
-  return true;
-}
 
 // Four 8 x 8 matrices of 16-bit elements from shared memory (ldmatrix).
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -1302,24 +1218,6 @@ int prepare_kernel(int dev) {
     return -1;
   slot.store(per_sm, std::memory_order_relaxed);
   return per_sm;
-}
-
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-struct WsLayout {
-  size_t seg_count, group_count, part_ml, part_o, total;
-};
-
-WsLayout layout(int64_t B, int64_t Hkv, int64_t G, int64_t W) {
-  WsLayout l;
-  const int64_t segs = B * Hkv;
-  const int64_t slots = segs + W;
-  l.seg_count = 256;
-  l.group_count = l.seg_count + align256(static_cast<size_t>(segs) * sizeof(int));
-  l.part_ml = l.group_count + align256(static_cast<size_t>(slots) * sizeof(int));
-  l.part_o = l.part_ml + align256(static_cast<size_t>(slots * G) * sizeof(float2));
-  l.total = l.part_o + align256(static_cast<size_t>(slots * G * kDim) * sizeof(float));
-  return l;
 }
 
 int auto_splits(int wave, int B, int Hkv) {

@@ -17,7 +17,8 @@ import torch
 from . import (fpk_decode_append_check_bf16, fpk_decode_append_check_fp8, fpk_decode_step_bf16,
                fpk_decode_step_fp8, fpk_decode_workspace_bytes, fpk_kv_append_bf16, fpk_kv_append_fp8,
                fpk_kv_prefill_bf16, fpk_kv_prefill_fp8, fpk_page_tags_bump,
-               fpk_page_tags_validate, fpk_paged_decode_attn_bf16, fpk_paged_decode_attn_fp8)
+               fpk_page_tags_validate, fpk_paged_decode_attn_bf16, fpk_paged_decode_attn_fp8,
+               fpk_paged_decode_attn_fp8_tc)
 
 NAN_E4M3 = 0x7F          # e4m3 NaN code: fills slots no token was written to
 NAN_BF16 = 0x7FC0
@@ -51,9 +52,13 @@ def _arena(device, specs):
 
 
 class DecodePool:
-    def __init__(self, wl, fp8: bool = True, device="cuda", num_splits: int | None = None):
+    def __init__(self, wl, fp8: bool = True, device="cuda", num_splits: int | None = None,
+                 tensor_cores: bool = False):
         self.wl = wl
         self.fp8 = fp8
+        # FP8 attention on the tcgen05 tensor cores (fpk_paged_decode_attn_fp8_tc)
+        # instead of the warp-level kernel; attend() only
+        self.tensor_cores = tensor_cores
         self.device = torch.device(device)
         dev = self.device
         n = 2 * wl.num_pages * wl.Hkv * wl.page_size * wl.D      # K and V of every slot
@@ -174,9 +179,9 @@ class DecodePool:
         kw = dict(Hkv=wl.Hkv, page_size=wl.page_size, num_pages=wl.num_pages,
                   sm_scale=wl.sm_scale, num_splits=ns, stream=stream)
         if self.fp8:
-            fpk_paged_decode_attn_fp8(self.q, self.kv_pool, self.k_scale, self.v_scale,
-                                      self.page_table, self.seq_lens, mask, self.out, self.lse,
-                                      self.workspace, **kw)
+            attn = fpk_paged_decode_attn_fp8_tc if self.tensor_cores else fpk_paged_decode_attn_fp8
+            attn(self.q, self.kv_pool, self.k_scale, self.v_scale, self.page_table, self.seq_lens,
+                 mask, self.out, self.lse, self.workspace, **kw)
         else:
             fpk_paged_decode_attn_bf16(self.q, self.kv_pool, self.page_table,
                                        self.seq_lens, mask, self.out, self.lse, self.workspace, **kw)

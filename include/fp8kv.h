@@ -330,6 +330,37 @@ int fpk_paged_decode_attn_fp8(const void* q, const uint8_t* kv_pool,
                               int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
                               void* stream);
 
+/*
+ * Variant of fpk_paged_decode_attn_fp8 on the fifth-generation tensor cores
+ * (tcgen05.mma of kind f8f6f4, accumulators in tensor memory): same
+ * arguments, same results within the same tolerance, same workspace
+ * (fpk_decode_workspace_bytes covers it), same fail-closed rules.
+ * Source: "Perche le cache piu piccole di Cloudflare battono la velocita pura"
+ * (the decode kernel reads the FP8 cache and converts it as it reads): here
+ * the e4m3 codes of K and V enter the MMAs as they lie in shared memory, and
+ * the query and the softmax weights enter as four e4m3 parts each
+ * (x = c0 + c1/16 + c2/256 + c3/4096, 16 significant bits), recombined in
+ * fp32 from the accumulators.
+ * Differences from fpk_paged_decode_attn_fp8:
+ *   - num_splits == 0 picks one wave of CTAs (at most 16 splits per
+ *     (request, kv head)), or, when every non-empty request has the same
+ *     length, the uniform rule of fpk_paged_decode_attn_fp8; mixed-length
+ *     small batches keep equal-size splits (no segment-aligned partition);
+ *   - a split count above the batch's 16-token tile count is lowered to it;
+ *   - every split of a segment is merged in one level (no groups above 16);
+ *   - the pool may hold at most 2^31 rows of 128 bytes (256 GiB), else
+ *     FPK_EUNSUPPORTED.
+ * Bit-identical on repeated calls with the same inputs and split count.
+ */
+int fpk_paged_decode_attn_fp8_tc(const void* q, const uint8_t* kv_pool,
+                                 const float* k_scale, const float* v_scale,
+                                 const int32_t* page_table, int32_t max_pages,
+                                 const int32_t* seq_lens, const uint8_t* abort_mask,
+                                 float* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 int32_t num_splits, float sm_scale, int32_t B, int32_t Hq,
+                                 int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages,
+                                 void* stream);
+
 /* BF16-cache variant of fpk_paged_decode_attn_fp8: same semantics with
  * kv_pool holding bf16 values (no scales). */
 int fpk_paged_decode_attn_bf16(const void* q, const void* kv_pool,

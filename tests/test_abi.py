@@ -116,6 +116,8 @@ def test_cpu_tensors_are_refused(lib):
                                                        page_size=ps),
         "attn_fp8": lambda: fpk.fpk_paged_decode_attn_fp8(q, pool8, sc, sc, pt, lens, None, out, lse,
                                                           ws, sm_scale=0.1, **geo),
+        "attn_fp8_tc": lambda: fpk.fpk_paged_decode_attn_fp8_tc(q, pool8, sc, sc, pt, lens, None, out,
+                                                                lse, ws, sm_scale=0.1, **geo),
         "attn_bf16": lambda: fpk.fpk_paged_decode_attn_bf16(q, pool16, pt, lens, None, out, lse, ws,
                                                             sm_scale=0.1, **geo),
         "step_fp8": lambda: fpk.fpk_decode_step_fp8(kv, kv, pool8, sc, sc, pt, lens, tags, exp, mask,
@@ -171,6 +173,23 @@ def test_attention_argument_errors_before_any_device_call():
     assert bf16(Hq=15) == EINVAL and bf16(D=256) == EUNSUP
     assert bf16(out=A + 4) == EINVAL and bf16(ws=None) == EINVAL
     assert bf16(B=0, q=None) == OK
+
+    # the tensor-core variant checks the same arguments, and rejects pools
+    # whose 128-byte rows exceed 32-bit tensor-map coordinates
+    def tc(q=A, kv=A, ks=A, vs=A, pt=A, lens=A, out=A, ws=A, B=2, Hq=16, Hkv=2, D=128, ps=16,
+           num_pages=8, splits=0):
+        return lib.fpk_paged_decode_attn_fp8_tc(q, kv, ks, vs, pt, 4, lens, None, out, None, ws,
+                                                1 << 20, splits, 0.1, B, Hq, Hkv, D, ps, num_pages,
+                                                None)
+
+    assert tc(B=0, q=None, kv=None, out=None, ws=None) == OK
+    assert tc(Hq=15) == EINVAL and tc(B=-1) == EINVAL and tc(splits=-1) == EINVAL
+    assert tc(D=64) == EUNSUP and tc(ps=24) == EUNSUP and tc(Hq=32, Hkv=2) == EUNSUP
+    assert tc(num_pages=1 << 23, Hkv=8, Hq=64, ps=16) == EUNSUP     # 2^31 rows of 128 bytes
+    for name in ("q", "kv", "ks", "vs", "pt", "lens", "out", "ws"):
+        assert tc(**{name: None}) == EINVAL, name
+    assert tc(q=A + 2) == EINVAL and tc(kv=A + 8) == EINVAL and tc(out=A + 4) == EINVAL
+    assert tc(ws=A + 16) == EINVAL
 
     # the allocation-free entry point checks the same arguments (it has no
     # workspace) before it looks up its scratch or clears it
