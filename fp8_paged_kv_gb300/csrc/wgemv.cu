@@ -34,6 +34,11 @@ constexpr int kW8SliceBytes = 16 * kGroupK;
 constexpr int kGemvWarps = 8;
 constexpr int kGemvThreads = kGemvWarps * 32;
 constexpr int kKChunk = 2048;  // k per CTA (split-K)
+// INT4 weights at one token: the largest K one CTA takes whole (its 64 rows'
+// group scales fill the same table as 128 rows of a kKChunk chunk, twice over)
+constexpr int kWholeKMax = 8192;
+constexpr int kGscaleEntries = (kGemvWarps / 2) * 16 * (kWholeKMax / kGroupK);
+static_assert(kGemvWarps * 16 * (2 * kKChunk / kGroupK) <= kGscaleEntries, "the scale table holds a chunk's too");
 constexpr int kXPad = 16;      // bf16 of padding per staged activation row
 
 __device__ __forceinline__ int w4_nibble_index(int s, int j) {
@@ -200,15 +205,21 @@ __device__ __forceinline__ uint32_t w4_pair_to_f16x2(uint32_t v, uint32_t mask, 
 // for INT4 the activations at k = 2, 3 (mod 4) are staged divided by 16,
 // because the weights there come out of the nibble trick multiplied by 16.
 // kNT n8 tiles of batch columns (B <= 8 kNT); only the B real rows are staged.
-// kRing groups of ring per warp (kRing - 1 in flight).
-template <bool kW4, int kNT, int kRing>
+// kRing groups of ring per warp (kRing - 1 in flight).  kSplit == 2: the CTA
+// takes the whole K for 4 slices, warps w and w + 4 one half of K each, and
+// the halves are summed in shared memory -- y is written once, without
+// atomics or a zeroing pass.
+template <bool kW4, int kNT, int kRing, int kSplit = 1>
 __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   extern __shared__ __align__(16) uint8_t gsm[];
   constexpr int kSliceBytes = kW4 ? kW4SliceBytes : kW8SliceBytes;
   constexpr int kRingBytesPerWarp = kRing * kSliceBytes;
   constexpr int kVec = kSliceBytes / 512;                 // 16-byte words per lane per group
+  constexpr int kSlicesPerCta = kGemvWarps / kSplit;
+  static_assert(kRingBytesPerWarp >= 32 * 16 * kNT, "a warp's ring holds its lanes' partial sums");
   __shared__ float s_unscale[8 * kNT];                    // 2^-e_b per staged row
-  __shared__ uint16_t s_gscale[kGemvWarps * 16][kKChunk / kGroupK];  // INT4 group scales of the CTA's rows
+  // INT4 group scales of the CTA's rows, [row][group of the CTA's chunk]
+  __shared__ uint16_t s_gscale[kW4 ? kGscaleEntries : 1];
   const int G = a.K / kGroupK;
   const int k0 = blockIdx.y * a.kc;
   const int kc = min(a.kc, a.K - k0);
@@ -217,14 +228,19 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   const int xstride = kc + kXPad;
   const int rows = min(a.B, 8 * kNT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slice = blockIdx.x * kGemvWarps + warp;
+  const int wslot = warp % kSlicesPerCta;  // slice of the CTA
+  const int khalf = warp / kSlicesPerCta;  // part of the CTA's K this warp takes
+  const int slice = blockIdx.x * kSlicesPerCta + wslot;
   const bool has_slice = slice < a.N / 16;
+  const int wng = ng / kSplit;             // this warp's groups
+  const int wg0 = khalf * wng;             // its first group within the CTA's chunk
   uint16_t* xs = reinterpret_cast<uint16_t*>(gsm + kGemvWarps * kRingBytesPerWarp);
   // ---- this warp's weight stream starts first
-  const uint8_t* wp = a.codes + (static_cast<int64_t>(has_slice ? slice : 0) * G + g0) * kSliceBytes + 16 * lane;
+  const uint8_t* wp =
+      a.codes + (static_cast<int64_t>(has_slice ? slice : 0) * G + g0 + wg0) * kSliceBytes + 16 * lane;
   const uint32_t ring = smem_addr(gsm + warp * kRingBytesPerWarp) + 16 * lane;
   auto issue = [&](int gi) {
-    if (has_slice && gi < ng) {
+    if (has_slice && gi < wng) {
 #pragma unroll
       for (int i = 0; i < kVec; ++i)
         cp_async16(ring + (gi % kRing) * kSliceBytes + 512 * i, wp + static_cast<int64_t>(gi) * kSliceBytes + 512 * i);
@@ -236,10 +252,10 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   // ---- the CTA's INT4 group scales for this chunk (ng per row; a row's run
   // of scales is not 16-byte aligned in general, so element by element)
   if (kW4) {
-    for (int i = threadIdx.x; i < kGemvWarps * 16 * ng; i += kGemvThreads) {
+    for (int i = threadIdx.x; i < kSlicesPerCta * 16 * ng; i += kGemvThreads) {
       const int rrow = i / ng, gi = i - rrow * ng;
-      const int row = blockIdx.x * kGemvWarps * 16 + rrow;
-      s_gscale[rrow][gi] = row < a.N ? __ldg(a.gscales + static_cast<int64_t>(row) * G + g0 + gi) : 0;
+      const int row = blockIdx.x * kSlicesPerCta * 16 + rrow;
+      s_gscale[i] = row < a.N ? __ldg(a.gscales + static_cast<int64_t>(row) * G + g0 + gi) : 0;
     }
   }
   // ---- stage the chunk's activations: every thread takes the 8 values
@@ -247,20 +263,22 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   // rows go out before any reduction, then the row's largest |x| (bit
   // patterns, non-finite as 0) per warp, then the scaled f16 copy
   __shared__ uint32_t s_wmax[8 * kNT][kGemvWarps];
-  const bool has_item = static_cast<int>(threadIdx.x) < kc / 8;
+  // items of 8 values: thread tid takes tid, tid + kGemvThreads, ...
   {
     uint32_t m2[8 * kNT];
 #pragma unroll
     for (int b = 0; b < 8 * kNT; ++b) {
       m2[b] = 0u;
-      if (b < rows && has_item) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0) + threadIdx.x);
-        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+      for (int item = threadIdx.x; item < kc / 8; item += kGemvThreads) {
+        if (b < rows) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0) + item);
+          const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t u = ws[q] & 0x7FFF7FFFu;
-          u &= __vcmpltu2(u, 0x7F807F80u);
-          m2[b] = __vmaxu2(m2[b], u);
+          for (int q = 0; q < 4; ++q) {
+            uint32_t u = ws[q] & 0x7FFF7FFFu;
+            u &= __vcmpltu2(u, 0x7F807F80u);
+            m2[b] = __vmaxu2(m2[b], u);
+          }
         }
       }
     }
@@ -282,28 +300,30 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
       const int e = mb == 0 ? 0 : min(max(14 - ilogbf(__uint_as_float(mb << 16)), -126), 126);
       const float sc = __int_as_float((127 + e) << 23);
       if (threadIdx.x == 0) s_unscale[b] = __int_as_float((127 - e) << 23);
-      if (has_item) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0) + threadIdx.x);
-        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
+      for (int item = threadIdx.x; item < kc / 8; item += kGemvThreads) {
+        {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0) + item);
+          const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          // elements 8 tid + 2q, + 1: k mod 4 = 2q mod 4, 2q mod 4 + 1
-          const float f = (kW4 && (q & 1)) ? sc * 0.0625f : sc;
-          o[q] = pack_f16x2(__uint_as_float(ws[q] << 16) * f, __uint_as_float(ws[q] & 0xFFFF0000u) * f);
+          for (int q = 0; q < 4; ++q) {
+            // elements 8 item + 2q, + 1: k mod 4 = 2q mod 4, 2q mod 4 + 1
+            const float f = (kW4 && (q & 1)) ? sc * 0.0625f : sc;
+            o[q] = pack_f16x2(__uint_as_float(ws[q] << 16) * f, __uint_as_float(ws[q] & 0xFFFF0000u) * f);
+          }
+          *reinterpret_cast<uint4*>(xs + b * xstride + 8 * item) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *reinterpret_cast<uint4*>(xs + b * xstride + 8 * threadIdx.x) = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
   __syncthreads();
-  if (!has_slice) {
+  if (kSplit == 1 && !has_slice) {
     cp_async_wait<0>();
     return;
   }
   const int rr = lane >> 2, t = lane & 3;
   const int row0 = 16 * slice + rr, row1 = row0 + 8;
-  const int lrow0 = 16 * warp + rr, lrow1 = lrow0 + 8;  // rows within the CTA's scale table
+  const int lrow0 = 16 * wslot + rr, lrow1 = lrow0 + 8;  // rows within the CTA's scale table
 
   float acc[kNT][4];
 #pragma unroll
@@ -313,12 +333,12 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   // only, and the columns past B are never written out
   const uint16_t* xcol[kNT];
 #pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) xcol[nt] = xs + min(8 * nt + rr, rows - 1) * xstride + 4 * t;
+  for (int nt = 0; nt < kNT; ++nt) xcol[nt] = xs + min(8 * nt + rr, rows - 1) * xstride + kGroupK * wg0 + 4 * t;
   // nibble masks, the f16 magic 1024 and the biases, in registers
   const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
   const uint32_t blo = 0x64086408u, bhi = 0x64806480u;  // 1032, 1152
-  const uint16_t* gsc0 = &s_gscale[lrow0][0];
-  const uint16_t* gsc1 = &s_gscale[lrow1][0];
+  const uint16_t* gsc0 = &s_gscale[kW4 ? lrow0 * ng + wg0 : 0];
+  const uint16_t* gsc1 = &s_gscale[kW4 ? lrow1 * ng + wg0 : 0];
 
   // ring bookkeeping by running offsets: group gi is read from slot rd; the
   // group kRing - 1 ahead is written into the slot the previous group left
@@ -326,12 +346,12 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   const uint8_t* ring_ld = gsm + warp * kRingBytesPerWarp + 16 * lane;
   const uint8_t* gsrc = wp + static_cast<int64_t>(kRing - 1) * kSliceBytes;
   uint32_t rd = 0, wr = (kRing - 1) * kSliceBytes;
-  for (int gi = 0; gi < ng; ++gi) {
+  for (int gi = 0; gi < (has_slice ? wng : 0); ++gi) {
     cp_async_wait<kRing - 2>();  // group gi has landed (this lane's words)
     uint4 cur[kVec];
 #pragma unroll
     for (int i = 0; i < kVec; ++i) cur[i] = *reinterpret_cast<const uint4*>(ring_ld + rd + 512 * i);
-    if (gi + kRing - 1 < ng) {
+    if (gi + kRing - 1 < wng) {
 #pragma unroll
       for (int i = 0; i < kVec; ++i) cp_async16(ring + wr + 512 * i, gsrc + 512 * i);
     }
@@ -396,6 +416,26 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
     }
   }
   cp_async_wait<0>();
+  if (kSplit == 2) {
+    // the second half's sums go through its warp's ring (every copy of it
+    // has landed and been read); the first half adds them
+    float* part = reinterpret_cast<float*>(gsm + (wslot + kSlicesPerCta) * kRingBytesPerWarp) + 4 * kNT * lane;
+    if (khalf == 1) {
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+        *reinterpret_cast<float4*>(part + 4 * nt) = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+    }
+    __syncthreads();
+    if (khalf == 1 || !has_slice) return;
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      const float4 o = *reinterpret_cast<const float4*>(part + 4 * nt);
+      acc[nt][0] += o.x;
+      acc[nt][1] += o.y;
+      acc[nt][2] += o.z;
+      acc[nt][3] += o.w;
+    }
+  }
   float r0s = 1.f, r1s = 1.f;
   if (!kW4) {
     r0s = __ldg(a.rscales + row0);
@@ -595,14 +635,22 @@ int gemv_entry(const void* x, const uint8_t* codes, const void* gscales, const f
   // slower: each CTA's staging and ring fill then cover too few groups; so
   // was summing the K chunks of a row block in a thread-block cluster instead
   // of atomics into a zeroed y: 41.0 against 36.8 us at one token.)
-  const int kc = K < kKChunk ? K : kKChunk;
+  // INT4 at one token with K up to 8192: one CTA per 4 slices over the
+  // whole K, the two halves of K summed in the CTA -- no split-K atomics,
+  // hence no zeroing of y before the kernel (a second launch per call)
+  const bool whole_k = kW4 && B == 1 && K % (2 * kGroupK) == 0 && K <= kWholeKMax;
+  // INT4 at two tokens: chunks of 2 kKChunk, one wave of CTAs at three per SM
+  // (measured at 28672 x 8192: 34.8 us against 44.0 with kKChunk)
+  const int chunk = whole_k ? K : kW4 && B == 2 ? 2 * kKChunk : kKChunk;
+  const int kc = K < chunk ? K : chunk;
   a.kc = kc;
   const int chunks = (K + kc - 1) / kc;
   a.atomic = chunks > 1;
   if (a.atomic && cudaMemsetAsync(y, 0, sizeof(float) * B * static_cast<size_t>(N), s) != cudaSuccess)
     return FPK_ECUDA;
   const int nt = B <= 8 ? 1 : 2;
-  const dim3 grid((N / 16 + kGemvWarps - 1) / kGemvWarps, chunks);
+  const int slices_per_cta = whole_k ? kGemvWarps / 2 : kGemvWarps;
+  const dim3 grid((N / 16 + slices_per_cta - 1) / slices_per_cta, chunks);
   if (B > 4) {
     // 5..16 tokens: the register-streaming kernel (measured faster there:
     // INT4 at 28672 x 8192, 8 tokens 43 against 50 us, 16 tokens 53 against 72 us)
@@ -614,13 +662,13 @@ int gemv_entry(const void* x, const uint8_t* codes, const void* gscales, const f
     rk<<<grid, kGemvThreads, rsm, s>>>(a);
     return checked_launch_status();
   }
-  // 1..4 tokens: the landing-ring kernel; ring groups per warp -- INT4 8
-  // (B <= 2) or 6, e4m3 4 or 3
-  const int ring = kW4 ? (B <= 2 ? 8 : 6) : (B <= 2 ? 4 : 3);
+  // 1..4 tokens: the landing-ring kernel; ring groups per warp -- INT4 6
+  // (three CTAs per SM), e4m3 4 or 3
+  const int ring = kW4 ? 6 : (B <= 2 ? 4 : 3);
   const size_t smem = static_cast<size_t>(kGemvWarps) * ring * (kW4 ? kW4SliceBytes : kW8SliceBytes) +
                       static_cast<size_t>(B) * (kc + kXPad) * sizeof(uint16_t);
   void (*kern)(GemvArgs);
-  if constexpr (kW4) kern = B <= 2 ? wgemv_kernel<true, 1, 8> : wgemv_kernel<true, 1, 6>;
+  if constexpr (kW4) kern = whole_k ? wgemv_kernel<true, 1, 6, 2> : wgemv_kernel<true, 1, 6>;
   else kern = B <= 2 ? wgemv_kernel<false, 1, 4> : wgemv_kernel<false, 1, 3>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)

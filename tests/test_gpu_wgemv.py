@@ -85,7 +85,7 @@ def _tol(wd, x, K):
 
 
 @pytest.mark.parametrize("B", [1, 3, 8, 9, 16])
-@pytest.mark.parametrize("N,K", [(16, 128), (144, 2048), (64, 2176), (32, 4352)])
+@pytest.mark.parametrize("N,K", [(16, 128), (144, 2048), (64, 2176), (32, 4352), (48, 8192)])
 def test_w4_gemv_within_bound(B, N, K):
     wb = _weights(7 * B + K, N, K, specials=True)
     g = np.random.default_rng(B + N)
