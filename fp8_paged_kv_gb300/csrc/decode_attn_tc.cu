@@ -481,66 +481,76 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == kMmaWarp && !bad_start) {
     // ======================= MMA warp (one issuing thread) =======================
-    Cursor cur = start;
-    Piece p;
-    uint32_t j = 0, qn = 0;
-    bool ok = true;
-    int ab_r = -1, q_seg = -1;
-    bool ab = false;
-    const uint32_t tS = tmem, tO = tmem + 2 * kTcN;
-    const uint32_t qaddr = sbase + kOffQ;
-    // O^T = V^T P^T of block i: V blocks K-major without swizzle (core
-    // matrices of 8 dims x 16 tokens; 128 B apart along the dims, 2 KiB
-    // apart along the tokens), P K-major without swizzle (core matrices of 8
-    // columns x 16 tokens; 128 B along the columns, 512 B along the tokens)
-    auto pv = [&](uint32_t i) -> bool {
-      bool got = true;
-      if (lane == 0) {
-        const uint32_t sb = i & 1, u = i >> 1;
-        const uint32_t ob = i % kOBufs, ou = i / kOBufs;
-        got = mbar_wait(bar(kBarPFull + sb), u & 1, a.status);
-        if (got && ou > 0) got = mbar_wait(bar(kBarOFree + ob), (ou - 1) & 1, a.status);
-        if (got) {
-          tc_fence_after();
-          const uint32_t vaddr = sbase + kOffV + (i % kStagesV) * kSlotBytes;
-          const uint32_t paddr = sbase + kOffP + sb * kTcPBytes;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(vaddr + kk * 2 * kTile * kDim, kTile * kDim, 128, 0);
-            const uint64_t bd = smem_desc(paddr + kk * 2 * 512, 512, 128, 0);
-            mma_e4m3(tO + ob * kTcN, ad, bd, kk > 0);
+    // Two queues, issued as they become ready: S^T = K Q^T of the next block
+    // (its K rows landed, its S buffer read by the consumers, and for the
+    // first block of a new segment the query parts written), and O^T = V^T P^T
+    // of the oldest block whose P is written (and whose O buffer is free).  A
+    // group's next S is then computed while the group is still on its
+    // current block.  One thread polls the barriers, bounded like every wait.
+    if (lane == 0) {
+      Cursor cur = start;
+      Piece p;
+      bool ok = true, more = true, have_piece = false, need_q = false;
+      int ab_r = -1, q_seg = -1;
+      bool ab = false;
+      uint32_t qn = 0, jq = 0, jp = 0, piece_end = 0;
+      const uint32_t tS = tmem, tO = tmem + 2 * kTcN;
+      const uint32_t qaddr = sbase + kOffQ;
+      auto advance = [&]() {
+        while (more) {
+          if (!next_piece(cur, a, T, W, p)) {
+            more = false;
+            return;
           }
-          mma_commit(bar(kBarOFull + ob));
-          mma_commit(bar(kBarEmptyV + i % kStagesV));
+          if (p.r != ab_r) {
+            ab_r = p.r;
+            ab = is_aborted(a, p.r);
+          }
+          if (ab) continue;
+          const int seg = p.r * a.Hkv + p.h;
+          need_q = seg != q_seg;
+          q_seg = seg;
+          piece_end = jq + static_cast<uint32_t>((p.t1 - p.t0 + kBlkTiles - 1) / kBlkTiles);
+          have_piece = true;
+          return;
         }
-      }
-      return __shfl_sync(kFull, got, 0);
-    };
-    while (ok && next_piece(cur, a, T, W, p)) {
-      if (p.r != ab_r) {
-        ab_r = p.r;
-        ab = is_aborted(a, p.r);
-      }
-      if (ab) continue;
-      const int seg = p.r * a.Hkv + p.h;
-      if (seg != q_seg) {
-        q_seg = seg;
-        bool got = true;
-        if (lane == 0) got = mbar_wait(bar(kBarQFull), qn & 1, a.status);
-        ++qn;
-        if (!__shfl_sync(kFull, got, 0)) {
-          ok = false;
-          break;
+      };
+      advance();
+      uint64_t t0 = global_timer_ns();
+      uint32_t spins = 0;
+      while (ok && (have_piece || jp < jq)) {
+        bool progress = false;
+        if (jp < jq) {
+          // O^T = V^T P^T of block jp: V blocks K-major without swizzle (core
+          // matrices of 8 dims x 16 tokens; 128 B apart along the dims, 2 KiB
+          // apart along the tokens), P K-major without swizzle (core matrices
+          // of 8 columns x 16 tokens; 128 B along the columns, 512 B along
+          // the tokens)
+          const uint32_t sb = jp & 1, u = jp >> 1, ob = jp % kOBufs, ou = jp / kOBufs;
+          if (mbar_test(bar(kBarPFull + sb), u & 1) && (ou == 0 || mbar_test(bar(kBarOFree + ob), (ou - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t vaddr = sbase + kOffV + (jp % kStagesV) * kSlotBytes;
+            const uint32_t paddr = sbase + kOffP + sb * kTcPBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc(vaddr + kk * 2 * kTile * kDim, kTile * kDim, 128, 0);
+              const uint64_t bd = smem_desc(paddr + kk * 2 * 512, 512, 128, 0);
+              mma_e4m3(tO + ob * kTcN, ad, bd, kk > 0);
+            }
+            mma_commit(bar(kBarOFull + ob));
+            mma_commit(bar(kBarEmptyV + jp % kStagesV));
+            ++jp;
+            progress = true;
+          }
         }
-      }
-      const int nblk = (p.t1 - p.t0 + kBlkTiles - 1) / kBlkTiles;
-      for (int blk = 0; blk < nblk; ++blk, ++j) {
-        bool got = true;
-        if (lane == 0) {
-          const uint32_t ks = j % kStagesK, kround = j / kStagesK, sb = j & 1, u = j >> 1;
-          got = mbar_wait(bar(kBarFullK + ks), kround & 1, a.status);
-          if (got && u > 0) got = mbar_wait(bar(kBarSFree + sb), (u - 1) & 1, a.status);
-          if (got) {
+        if (have_piece) {
+          if (need_q && mbar_test(bar(kBarQFull), qn & 1)) {
+            ++qn;
+            need_q = false;
+          }
+          const uint32_t ks = jq % kStagesK, kround = jq / kStagesK, sb = jq & 1, u = jq >> 1;
+          if (!need_q && mbar_test(bar(kBarFullK + ks), kround & 1) &&
+              (u == 0 || mbar_test(bar(kBarSFree + sb), (u - 1) & 1))) {
             tc_fence_after();
             // S^T = K Q^T: K rows and query parts K-major, 128-byte swizzle
             // (8-row groups 1024 B apart); each K step of 32 advances 32 B
@@ -553,20 +563,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             mma_commit(bar(kBarSFull + sb));
             mma_commit(bar(kBarEmptyK + ks));
+            if (++jq == piece_end) {
+              have_piece = false;
+              advance();
+            }
+            progress = true;
           }
         }
-        if (!__shfl_sync(kFull, got, 0) || (blk > 0 && !pv(j - 1))) {
+        if (progress) {
+          t0 = global_timer_ns();
+          spins = 0;
+        } else if ((++spins & 255u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(a.status, kStatusWaitTimeout);
           ok = false;
-          break;
         }
       }
-      if (!ok || !pv(j - 1)) {
-        ok = false;
-        break;
-      }
-    }
-    // every MMA issued has completed before the tensor memory is freed
-    if (lane == 0) {
+      // every MMA issued has completed before the tensor memory is freed
       mma_commit(bar(kBarDone));
       mbar_wait(bar(kBarDone), 0, a.status);
     }
@@ -753,6 +765,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             m[h] = mn;
           }
         }
+        // ---- this group's previous block's O, before its P buffer is
+        // rewritten: the wait for that O is the wait for the PV MMA that read
+        // the buffer (the MMA thread may compute this block's S before it)
+        if (have_prev && !accumulate(j - 2, alpha_prev)) {
+          ok = false;
+          break;
+        }
+        have_prev = true;
+#pragma unroll
+        for (int h = 0; h < kHalfHeads; ++h) alpha_prev[h] = alpha[h];
         // ---- P = e4m3 parts of 256 p into this group's P buffer (K-major,
         // core matrices of 8 columns x 16 tokens)
         {
@@ -805,14 +827,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarPFull + grp));
-        // ---- this group's previous block's O
-        if (have_prev && !accumulate(j - 2, alpha_prev)) {
-          ok = false;
-          break;
-        }
-        have_prev = true;
-#pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) alpha_prev[h] = alpha[h];
       }
       if (!ok) break;
       // this group's last block of the piece (j - 1 or j - 2 by parity)
