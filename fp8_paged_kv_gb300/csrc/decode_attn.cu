@@ -128,6 +128,16 @@ struct Members {
   bool dense;
 };
 
+// Atomic add with acquire-release semantics at GPU scope (returns the old
+// value): the writes that happen before it are visible to the thread whose
+// atomic reads its result, and the caller sees the writes released by the
+// atomics it reads.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Four 8 x 8 matrices of 16-bit elements from shared memory (ldmatrix).
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                             uint32_t& r3) {
@@ -553,17 +563,16 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     ++cphase;
     return __all_sync(kFull, got);
   };
-  // Arrival ticket on a counter in global memory: every partial write of this
-  // CTA is fenced first; returns 1 for the arrival that completes `count`,
-  // 0 for the others, -1 if a barrier gave up.  Nothing ever waits on another
-  // CTA.
+  // Arrival ticket on a counter in global memory: one acquire-release atomic
+  // by consumer thread 0 after a barrier of the consumer warps, so every
+  // partial this CTA wrote before the barrier is visible to the CTA whose
+  // atomic completes `count`, and that CTA, after its own barrier, sees every
+  // other CTA's partials (no thread-wide fences); returns 1 for the arrival
+  // that completes `count`, 0 for the others, -1 if a barrier gave up.
+  // Nothing ever waits on another CTA.
   auto ticket = [&](int* ctr, int count, int arrivals) -> int {
-    __threadfence();
     if (!consumer_sync()) return -1;
-    if (ct_all == 0) {
-      s_last = atomicAdd(ctr, arrivals) + arrivals == count;
-      __threadfence();
-    }
+    if (ct_all == 0) s_last = atom_add_acq_rel_gpu(ctr, arrivals) + arrivals == count;
     if (!consumer_sync()) return -1;
     return s_last;
   };
@@ -593,7 +602,6 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     const int hh0 = min(hq0, a.G - 1);
     const int hh1 = min(hq0 + 4, a.G - 1);
     float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-    __threadfence();
     if (ct < kGroupMax) {
       s_M[ct] = kNegInf;
       s_W[ct] = 0.f;
