@@ -663,7 +663,7 @@ def run_gemv(args, rank, world):
     peak, peak_kind = measured_peaks()
     pts = []
     with ClockSampler(local_rank()) as clk:
-        for B in (1, 2, 4, 8, 16):
+        for B in (int(b) for b in args.gemv_batches.split(",")):
             x = torch.randn(B, K, device=dev, generator=g).to(torch.bfloat16)
             y = torch.empty(B, N, device=dev)
             row = {"batch": B}
@@ -690,6 +690,31 @@ def run_gemv(args, rank, world):
             "l2": L2Flush.NOTE, "clocks": clk.summary()}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_profile(args):
+    """One workload's attention kernel alone, for a profiler: the pool is written,
+    one decode step runs (cache write and tag check, then the warp-level
+    attention), then `--launches` attention launches of the chosen kernel
+    (FP8 or BF16 warp-level, or the FP8 tensor-core variant)."""
+    import fp8_paged_kv_gb300 as fpk
+    from fp8_paged_kv_gb300 import build as fbuild
+    from fp8_paged_kv_gb300.pool import DecodePool
+    from workloads import WORKLOADS
+    fbuild.build()
+    fpk.load_library()
+    wl = WORKLOADS[args.workload]()
+    pool = DecodePool(wl, fp8=args.profile != "bf16", device=torch.device("cuda", torch.cuda.current_device()),
+                      tensor_cores=args.profile == "tc")
+    pool.prefill()
+    pool.set_step(0)
+    pool.step()
+    for _ in range(args.launches):
+        pool.attend(use_mask=True)
+    torch.cuda.synchronize()
+    print(json.dumps({"mode": "profile", "kernel": args.profile, "workload": wl.name,
+                      "launches": args.launches, "status_word": fpk.fpk_decode_status(pool.workspace)}),
+          flush=True)
 
 
 def local_rank() -> int:
@@ -984,6 +1009,12 @@ def main():
                     help="INT4 vs e4m3 weight-only decode GEMV instead of the step benchmark")
     ap.add_argument("--gemv-n", type=int, default=28672)
     ap.add_argument("--gemv-k", type=int, default=8192)
+    ap.add_argument("--gemv-batches", default="1,2,4,8,16",
+                    help="decode batches of the --gemv leg (comma separated)")
+    ap.add_argument("--profile", choices=["fp8", "bf16", "tc"],
+                    help="run only the workload's attention (one decode step, then --launches "
+                         "attention launches), for a profiler")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -996,6 +1027,9 @@ def main():
         return
     if args.gemv:
         run_gemv(args, rank, world)
+        return
+    if args.profile:
+        run_profile(args)
         return
 
     import fp8_paged_kv_gb300 as fpk
