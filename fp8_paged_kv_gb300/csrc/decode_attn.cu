@@ -55,7 +55,8 @@ namespace fpk {
 namespace {
 
 constexpr int kMergeStride = 132;  // floats per head row of the merge buffer
-constexpr int kMergeBars = 6;      // merge_free, cbar, the three rounds of the two-slot merge, the four-slot one
+constexpr int kMergeBars = 7;      // merge_free, cbar, the three rounds of the two-slot merge, the four-slot one,
+                                   // the staged combine's copies
 constexpr int64_t kInflightBudget = 26ll << 20;  // bytes of ring stages over the grid (see Cfg)
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
@@ -232,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   // warps 0, 1 have read them (mrg1); warps 0, 1 have filled them (mrg2).
   // The four-slot merge: every warp has filled its slot (mrg4).
   const uint32_t mrg0 = cbar + 8, mrg1 = cbar + 16, mrg2 = cbar + 24, mrg4 = cbar + 32;
+  const uint32_t comb_bar = cbar + 40;  // the staged combine's bulk copies have landed
   // ---- prologue: total tiles and this CTA's start (block scan over requests)
   const int chunk = (a.B + kThreads - 1) / kThreads;
   const int rb = tid * chunk;
@@ -389,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     mbar_init(mrg1, 2);
     mbar_init(mrg2, 2);
     mbar_init(mrg4, kConsumerWarps);
+    mbar_init(comb_bar, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -585,7 +588,14 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   // indices past the group are clamped rather than branched on, so the loads
   // of several slots are in flight together.  The result goes to the final
   // output rows of (r, h) when dst < 0, else, as a partial, to slot dst.
-  auto combine = [&](const Members& mb, int n, int r, int h, int64_t dst) -> bool {
+  // Staged: once the CTA has no piece left its ring is idle, and when the n
+  // partials fit there they arrive by bulk copies (one per partial, issued
+  // from separate lanes) while the (m, l) pairs load: loads through the SM's
+  // load path keep only a few KiB in flight, and 16 partials (64 KiB) took
+  // about eight L2 round trips that way.  The sums are then taken from
+  // shared memory.
+  uint32_t comb_phase = 0;  // staged combines so far (the parity of comb_bar)
+  auto combine = [&](const Members& mb, int n, int r, int h, int64_t dst, bool ring_idle) -> bool {
     auto slot_of = [&](int k) -> int64_t {
       const int i = mb.i0 + k * mb.stride;
       return mb.seg + (mb.dense ? mb.w0 + i : worker_of(mb.xseg + i, T, W));
@@ -607,7 +617,66 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
       s_W[ct] = 0.f;
     }
     if (ct == 0) *s_dead = 0;
-    for (int c0 = 0; c0 < n; c0 += kChunk) {
+    const uint32_t pbytes = static_cast<uint32_t>(a.G) * kDim * 4;  // one partial
+    const bool staged = ring_idle && n <= kChunk && n * pbytes <= static_cast<uint32_t>(C::kRingBytes);
+    if (staged) {
+      if (c == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(comb_bar, n * pbytes);
+        __syncwarp();
+        // the partials were written through the generic proxy; the copies read them through the async one
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        const uint64_t pol = l2_policy_evict_first();
+        for (int i = lane; i < n; i += 32)
+          bulk_g2s(smem_addr(ring) + i * pbytes, a.part_o + slot_of(i) * a.G * kDim, pbytes, comb_bar, pol);
+      }
+      for (int e = ct; e < n * a.G; e += kConsumerWarps * 32) {
+        const int i = e / a.G;
+        const int hd = e - i * a.G;
+        s_w[i * kGroupMax + hd] = __ldcg(a.part_ml + slot_of(i) * a.G + hd);
+      }
+      const bool got = mbar_wait(comb_bar, comb_phase & 1, a.status);
+      ++comb_phase;
+      if (!__all_sync(kFull, got)) {
+        // the copies must land (bounded) before the CTA exits
+        if (c == 0 && lane == 0) mbar_wait(comb_bar, (comb_phase - 1) & 1, a.status);
+        return false;
+      }
+      if (!consumer_sync()) return false;
+      if (ct < a.G) {
+        float mn = kNegInf;
+        bool dd = false;
+        for (int i = 0; i < n; ++i) {
+          const float2 ml = s_w[i * kGroupMax + ct];
+          mn = fmaxf(mn, ml.x);
+          dd |= ml.y < 0.f;
+        }
+        float wsum = 0.f;
+        for (int i = 0; i < n; ++i) {
+          const float2 ml = s_w[i * kGroupMax + ct];
+          const float f = ml.x == kNegInf ? 0.f : fast_exp2(ml.x - mn);
+          wsum = fmaf(ml.y, f, wsum);
+          s_w[i * kGroupMax + ct].x = f;
+        }
+        s_M[ct] = mn;
+        s_W[ct] = wsum;
+        if (dd) *s_dead = 1;
+      }
+      if (!consumer_sync()) return false;
+      const float4* po = reinterpret_cast<const float4*>(ring);
+      for (int i = 0; i < n; ++i) {
+        const float f0 = s_w[i * kGroupMax + hh0].x;
+        const float f1 = s_w[i * kGroupMax + hh1].x;
+        const float4 v0 = po[(i * a.G + hh0) * (kDim / 4) + d4];
+        const float4 v1 = po[(i * a.G + hh1) * (kDim / 4) + d4];
+        acc0 = make_float4(fmaf(v0.x, f0, acc0.x), fmaf(v0.y, f0, acc0.y), fmaf(v0.z, f0, acc0.z),
+                           fmaf(v0.w, f0, acc0.w));
+        acc1 = make_float4(fmaf(v1.x, f1, acc1.x), fmaf(v1.y, f1, acc1.y), fmaf(v1.z, f1, acc1.z),
+                           fmaf(v1.w, f1, acc1.w));
+      }
+      // every thread has read the ring before a later combine of this CTA refills it
+      if (!consumer_sync()) return false;
+    }
+    for (int c0 = 0; !staged && c0 < n; c0 += kChunk) {
       const int nc = min(kChunk, n - c0);
       for (int e = ct; e < nc * a.G; e += kConsumerWarps * 32) {
         const int i = e / a.G;
@@ -754,13 +823,14 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     return q;
   };
   // the pending arrivals: ticket, and the combines they complete
-  auto flush = [&](Pending q) -> bool {
+  // (ring_idle: the CTA has no piece left, see combine)
+  auto flush = [&](Pending q, bool ring_idle) -> bool {
     int arrivals = q.k;
     for (;;) {
       const int last = ticket(q.ctr, q.n, arrivals);
       if (last < 0) return false;
       if (last == 0) return true;
-      if (!combine(q.mb, q.n, q.r, q.h, q.dst)) return false;
+      if (!combine(q.mb, q.n, q.r, q.h, q.dst, ring_idle)) return false;
       if (ct_all == 0) *q.ctr = 0;  // ready for the next call
       if (q.dst < 0) return true;
       // the group is folded into the slot of its first member: on to the
@@ -783,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
     if (pk > 0 && !same) {
       Pending q = pending_of(s_pend_piece, s_pend_seg);
       q.k = pk;
-      if (!flush(q)) return false;  // its barriers follow every thread's reads above
+      if (!flush(q, false)) return false;  // its barriers follow every thread's reads above
     } else if (!consumer_sync()) {
       return false;
     }
@@ -1201,7 +1271,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_decode_split_kernel(const A
   if (ok && consumer_sync() && s_pend_k > 0) {
     Pending q = pending_of(s_pend_piece, s_pend_seg);
     q.k = s_pend_k;
-    flush(q);
+    flush(q, true);
   }
 }
 
