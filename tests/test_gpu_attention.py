@@ -130,6 +130,21 @@ def test_mixed_small_batch_segment_aligned_splits(fp8, lens, abort_at):
 
 
 @pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("B", [18, 30])
+def test_mixed_batch_past_a_third_of_the_ctas(fp8, B):
+    # 18 and 30 requests of unequal lengths (144 and 240 segments, more than a
+    # third of a wave): the automatic count keeps splits of equal tile count
+    # over the whole batch, straddling segments; one request aborted
+    lens = [int(x) for x in rng_for(150 + B, "lens").integers(100, 3000, size=B)]
+    wl = custom(150 + B, B=B, Hq=64, Hkv=8, ps=16, prompt_lens=lens, steps=0, sigma=1.0,
+                outlier_frac=0.01)
+    abort = np.zeros(wl.B, np.uint8)
+    abort[B // 2] = 1
+    out, lse, ro, rl = _run_case(wl, fp8, 0, abort=abort, use_mask=True)
+    assert_attention_close(out, lse, ro, rl, f"mixed B={B} fp8={fp8}")
+
+
+@pytest.mark.parametrize("fp8", [True, False])
 def test_uneven_batch_of_whole_segment_size(fp8):
     # 30 x 8 segments, as above, but of uneven lengths: the host launches the
     # deep-ring FP8 variant for a batch that may run one whole segment per CTA;
