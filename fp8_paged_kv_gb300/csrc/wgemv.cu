@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   static_assert(kRingBytesPerWarp >= 32 * 16 * kNT, "a warp's ring holds its lanes' partial sums");
   __shared__ float s_unscale[8 * kNT];                    // 2^-e_b per staged row
   // INT4 group scales of the CTA's rows, [row][group of the CTA's chunk]
-  __shared__ uint16_t s_gscale[kW4 ? kGscaleEntries : 1];
+  __shared__ __align__(16) uint16_t s_gscale[kW4 ? kGscaleEntries : 1];
   const int G = a.K / kGroupK;
   const int k0 = blockIdx.y * a.kc;
   const int kc = min(a.kc, a.K - k0);
@@ -249,35 +249,71 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
   };
 #pragma unroll
   for (int gi = 0; gi < kRing - 1; ++gi) issue(gi);
-  // ---- the CTA's INT4 group scales for this chunk (ng per row; a row's run
-  // of scales is not 16-byte aligned in general, so element by element)
+  // ---- the CTA's INT4 group scales for this chunk (ng per row).  A row's
+  // run of scales starts on a 16-byte boundary when G, g0 and ng are
+  // multiples of 8: then 8 at a time, every thread's loads issued before any
+  // of its stores (one round trip); otherwise element by element.
   if (kW4) {
-    for (int i = threadIdx.x; i < kSlicesPerCta * 16 * ng; i += kGemvThreads) {
-      const int rrow = i / ng, gi = i - rrow * ng;
-      const int row = blockIdx.x * kSlicesPerCta * 16 + rrow;
-      s_gscale[i] = row < a.N ? __ldg(a.gscales + static_cast<int64_t>(row) * G + g0 + gi) : 0;
+    const int total = kSlicesPerCta * 16 * ng;
+    const int row_base = blockIdx.x * kSlicesPerCta * 16;
+    if (G % 8 == 0 && g0 % 8 == 0 && ng % 8 == 0 && (reinterpret_cast<uintptr_t>(a.gscales) & 15u) == 0) {
+      constexpr int kMaxV = kGscaleEntries / 8 / kGemvThreads;
+      const int per_row = ng / 8;
+      uint4 v[kMaxV];
+#pragma unroll
+      for (int u = 0; u < kMaxV; ++u) {
+        const int i = threadIdx.x + u * kGemvThreads;
+        const int rrow = i / per_row, q = i - rrow * per_row;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < total / 8 && row_base + rrow < a.N)
+          v[u] = __ldg(reinterpret_cast<const uint4*>(a.gscales + static_cast<int64_t>(row_base + rrow) * G + g0) + q);
+      }
+#pragma unroll
+      for (int u = 0; u < kMaxV; ++u) {
+        const int i = threadIdx.x + u * kGemvThreads;
+        if (i < total / 8) reinterpret_cast<uint4*>(s_gscale)[i] = v[u];
+      }
+    } else {
+      for (int i = threadIdx.x; i < total; i += kGemvThreads) {
+        const int rrow = i / ng, gi = i - rrow * ng;
+        const int row = row_base + rrow;
+        s_gscale[i] = row < a.N ? __ldg(a.gscales + static_cast<int64_t>(row) * G + g0 + gi) : 0;
+      }
     }
   }
-  // ---- stage the chunk's activations: every thread takes the 8 values
-  // 8 tid .. 8 tid + 7 of each row (kc / 8 <= kGemvThreads); the loads of all
-  // rows go out before any reduction, then the row's largest |x| (bit
-  // patterns, non-finite as 0) per warp, then the scaled f16 copy
+  // ---- stage the chunk's activations: items of 8 values, thread tid takes
+  // items tid, tid + kGemvThreads, ... of each row.  A row's loads all go out
+  // before any of them is used (one round trip); the raw bf16 go to their
+  // place in shared memory while the row's largest |x| (bit patterns,
+  // non-finite as 0) is taken per warp; after the block maximum every thread
+  // turns its own items into the scaled f16 copy in place.
   __shared__ uint32_t s_wmax[8 * kNT][kGemvWarps];
-  // items of 8 values: thread tid takes tid, tid + kGemvThreads, ...
+  constexpr int kMaxItems = kWholeKMax / 8 / kGemvThreads;  // items per thread and row
   {
     uint32_t m2[8 * kNT];
 #pragma unroll
     for (int b = 0; b < 8 * kNT; ++b) {
       m2[b] = 0u;
-      for (int item = threadIdx.x; item < kc / 8; item += kGemvThreads) {
-        if (b < rows) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0) + item);
-          const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+      if (b < rows) {
+        const uint4* xrow = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0);
+        uint4 v[kMaxItems];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t u = ws[q] & 0x7FFF7FFFu;
-            u &= __vcmpltu2(u, 0x7F807F80u);
-            m2[b] = __vmaxu2(m2[b], u);
+        for (int u = 0; u < kMaxItems; ++u) {
+          const int item = threadIdx.x + u * kGemvThreads;
+          v[u] = item < kc / 8 ? __ldg(xrow + item) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kMaxItems; ++u) {
+          const int item = threadIdx.x + u * kGemvThreads;
+          if (item < kc / 8) {
+            *reinterpret_cast<uint4*>(xs + b * xstride + 8 * item) = v[u];
+            const uint32_t ws[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w2 = ws[q] & 0x7FFF7FFFu;
+              w2 &= __vcmpltu2(w2, 0x7F807F80u);
+              m2[b] = __vmaxu2(m2[b], w2);
+            }
           }
         }
       }
@@ -300,9 +336,11 @@ __global__ void __launch_bounds__(kGemvThreads) wgemv_kernel(const GemvArgs a) {
       const int e = mb == 0 ? 0 : min(max(14 - ilogbf(__uint_as_float(mb << 16)), -126), 126);
       const float sc = __int_as_float((127 + e) << 23);
       if (threadIdx.x == 0) s_unscale[b] = __int_as_float((127 - e) << 23);
-      for (int item = threadIdx.x; item < kc / 8; item += kGemvThreads) {
-        {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(b) * a.K + k0) + item);
+#pragma unroll
+      for (int u = 0; u < kMaxItems; ++u) {
+        const int item = threadIdx.x + u * kGemvThreads;
+        if (item < kc / 8) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xs + b * xstride + 8 * item);
           const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
           uint32_t o[4];
 #pragma unroll
